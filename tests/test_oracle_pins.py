@@ -1,0 +1,643 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: brute force
+over the format tables, closed forms, invariants, special cases that reduce
+to a library routine (torch scaled_dot_product_attention in fp64, torch's
+float8_e4m3fn cast), or values derived from the pages' formulas.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import layout
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+E2M1_MAG = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def f32_neighbourhood(centres, span):
+    """All binary32 values within +-span ulps of each centre (both signs)."""
+    out = []
+    for c in centres:
+        b = np.array([c], np.float32).view(np.int32)[0]
+        ints = np.arange(b - span, b + span + 1, dtype=np.int64)
+        ints = ints[(ints >= 0) & (ints < 0x7F800000)]
+        v = ints.astype(np.int32).view(np.float32)
+        out += [v, -v]
+    return np.concatenate(out)
+
+
+def all_finite_bf16_as_f32():
+    u = np.arange(65536, dtype=np.uint32) << 16
+    f = u.view(np.float32)
+    return f[np.isfinite(f)]
+
+
+def brute_e2m1(x):
+    """Nearest E2M1 magnitude, ties to the even code index; sign bit kept."""
+    a = np.abs(x.astype(np.float64))
+    d = np.abs(a[:, None] - E2M1_MAG[None, :])
+    dmin = d.min(1, keepdims=True)
+    cand = d == dmin
+    idx = np.where(cand[:, ::2].any(1) & (cand.sum(1) > 1),
+                   np.argmax(cand & (np.arange(8) % 2 == 0), 1), np.argmax(cand, 1))
+    idx[a >= 6] = 7   # satfinite (the distance table loses resolution for huge inputs)
+    return (idx | (np.signbit(x) * 8)).astype(np.uint8)
+
+
+E4M3_POS = np.array([layout.E4M3[b] for b in range(0x7F)], np.float64)
+
+
+def brute_e4m3(s):
+    s = s.astype(np.float64)
+    d = np.abs(s[:, None] - E4M3_POS[None, :])
+    dmin = d.min(1, keepdims=True)
+    cand = d == dmin
+    idx = np.where(cand.sum(1) > 1, np.argmax(cand & (np.arange(0x7F) % 2 == 0), 1), np.argmax(cand, 1))
+    idx[s > 448] = 0x7E
+    return idx.astype(np.uint8)
+
+
+# ------------------------------------------------------- scalar encoders ---
+
+def test_e2m1_value_set():
+    vals = oracle.e2m1_value(np.arange(16))
+    assert list(vals[:8]) == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert list(vals[8:]) == [-0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+    assert np.signbit(vals[8])
+
+
+def test_e2m1_encode_brute_force():
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1, 1.5, 2, 3, 4, 6, 1e-30]
+    rng = np.random.default_rng(1)
+    x = np.concatenate([all_finite_bf16_as_f32(), f32_neighbourhood(mids, 4096),
+                        rng.uniform(-10, 10, 1_000_000).astype(np.float32),
+                        np.array([0.0, -0.0, 6.0, -6.0, 1e38, -1e38, 1e-45, -1e-45], np.float32)])
+    got = oracle.e2m1_encode(x)
+    exp = brute_e2m1(x)
+    assert np.array_equal(got, exp)
+    # exact ties resolve to the even code
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    assert list(oracle.e2m1_encode(ties)) == [0, 2, 2, 4, 4, 6, 6]
+    assert oracle.e2m1_encode(np.array([-0.1], np.float32))[0] == 0x8
+
+
+def test_e2m1_roundtrip():
+    v = oracle.e2m1_value(np.arange(16))
+    assert np.array_equal(oracle.e2m1_encode(v), np.arange(16, dtype=np.uint8))
+
+
+def test_e4m3_encode_brute_force():
+    mids = list((E4M3_POS[1:] + E4M3_POS[:-1]) / 2) + [448.0, 464.0, 2.0 ** -10, 2.0 ** -9]
+    rng = np.random.default_rng(2)
+    x = np.concatenate([all_finite_bf16_as_f32(), f32_neighbourhood(mids, 512),
+                        np.exp2(rng.uniform(-14, 10, 500_000)).astype(np.float32)])
+    x = np.abs(x)
+    got = oracle.e4m3_encode(x)
+    assert np.array_equal(got, brute_e4m3(x))
+    # saturation and underflow edges
+    assert oracle.e4m3_encode(np.array([1e30, 449, 2.0 ** -10, 2.0 ** -10 * 1.0001], np.float32)).tolist() == [
+        0x7E, 0x7E, 0, 1]
+
+
+def test_e4m3_matches_torch_cast():
+    rng = np.random.default_rng(3)
+    x = np.exp2(rng.uniform(-12, 8.8, 200_000)).astype(np.float32)
+    x = x[x <= 448]
+    t = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), t)
+
+
+def test_e4m3_values_and_roundtrip():
+    vals = oracle.e4m3_value(np.arange(0x7F))
+    assert vals[0x7E] == 448.0 and vals[1] == 2.0 ** -9 and vals[8] == 2.0 ** -6
+    assert np.array_equal(oracle.e4m3_encode(vals), np.arange(0x7F, dtype=np.uint8))
+    assert np.array_equal(vals.astype(np.float64), E4M3_POS)
+
+
+# -------------------------------------------------------- block quantizers ---
+
+def test_nvfp4_block_closed_forms():
+    # explicit bytes: amax = 6, g = 1
+    x = np.zeros(16, np.float32)
+    x[0] = 6.0
+    _, sb6, xh6 = oracle.nvfp4_block(x, 6, 1.0)
+    _, sb4, xh4 = oracle.nvfp4_block(x, 4, 1.0)
+    assert sb6 == 0x38 and sb4 == 0x3C   # 1.0 and 1.5
+    assert xh6[0] == 6.0 and xh4[0] == 6.0
+
+
+def test_nvfp4_block_grid_exact():
+    rng = np.random.default_rng(5)
+    for k in range(-4, 5):
+        for j in (-4, 0, 3):
+            x = (rng.choice(E2M1_MAG, 16) * rng.choice([-1, 1], 16)).astype(np.float32)
+            x[0] = 6.0
+            x = (x * 2.0 ** k).astype(np.float32)
+            g = float(2.0 ** j)
+            codes, sb, xh = oracle.nvfp4_block(x, 6, g)
+            assert layout.E4M3[sb] == 2.0 ** (k - j)
+            assert np.array_equal(xh, x)
+            assert oracle.block_sse(x, xh) == 0.0
+
+
+def test_nvfp4_block_nearest_and_bound():
+    """Given the chosen scale S, every code is the nearest reconstruction."""
+    rng = np.random.default_rng(6)
+    near_ties = 0
+    for trial in range(3000):
+        x = (rng.standard_normal(16) * np.exp(rng.uniform(-4, 4))).astype(np.float32)
+        g = float(np.float32(np.exp(rng.uniform(-6, 0))))
+        m = int(rng.choice([6, 4, 2]))
+        codes, sb, xh = oracle.nvfp4_block(x, m, g)
+        S = np.float64(np.float32(np.float32(layout.E4M3[sb]) * np.float32(g)))
+        rec = layout.E2M1[codes] * S
+        assert np.allclose(rec, xh, rtol=2 ** -23, atol=0)
+        assert np.all(np.abs(xh) <= 6 * S * (1 + 2 ** -23))
+        err_all = np.abs(x.astype(np.float64)[:, None] - (np.concatenate([E2M1_MAG, -E2M1_MAG]) * S)[None, :])
+        best = err_all.min(1)
+        mine = np.abs(x.astype(np.float64) - rec)
+        ok = mine <= best * (1 + 1e-6) + 1e-30
+        near_ties += int((~ok).sum())
+        # the only tolerated misses are within binary32 rounding of a tie
+        if not ok.all():
+            assert np.all(mine[~ok] - best[~ok] <= 4 * 2 ** -24 * np.abs(x[~ok]) + 1e-30)
+        # sign of each nonzero code follows the input
+        nz = layout.E2M1[codes] != 0
+        assert np.all(np.signbit(layout.E2M1[codes][nz]) == np.signbit(x[nz]))
+    assert near_ties < 30
+
+
+def test_nvfp4_block_power_of_two_covariance():
+    rng = np.random.default_rng(7)
+    for _ in range(500):
+        x = rng.standard_normal(16).astype(np.float32)
+        g = float(np.float32(rng.uniform(0.001, 0.01)))
+        m = int(rng.choice([6, 4, 2]))
+        c1, s1, x1 = oracle.nvfp4_block(x, m, g)
+        for k in (-3, 2, 5):
+            c2, s2, x2 = oracle.nvfp4_block((x * 2.0 ** k).astype(np.float32), m, float(np.float32(g * 2.0 ** k)))
+            assert np.array_equal(c1, c2) and s1 == s2
+            assert np.array_equal((x1 * 2.0 ** k).astype(np.float32), x2)
+
+
+def test_block_sse_tree():
+    rng = np.random.default_rng(8)
+    for n in (16, 32):
+        x = rng.standard_normal(n).astype(np.float32)
+        xh = (x + rng.standard_normal(n).astype(np.float32) * 0.1).astype(np.float32)
+        exact = float(np.sum((x.astype(np.float64) - xh.astype(np.float64)) ** 2))
+        assert abs(oracle.block_sse(x, xh) - exact) <= 8 * 2 ** -24 * exact
+        # an error in one element is fully counted
+        x2, xh2 = x.copy(), x.copy()
+        x2[n - 1], xh2[n - 1] = 1.0, 1.5
+        assert oracle.block_sse(x2, xh2) == 0.25
+
+
+def test_all_zero_blocks():
+    z = np.zeros(16, np.float32)
+    c, sb, xh = oracle.nvfp4_block(z, 6, 0.01)
+    assert sb == 0 and not c.any() and not xh.any()
+    m, c, sb, xh, e4, e6 = oracle.four_six_block(z, 0.01)
+    assert m == 6 and sb == 0 and not c.any()
+    e, c, sb, xh, ea, eb = oracle.mx_block(np.zeros(32, np.float32))
+    assert sb == 0 and not c.any()
+
+
+def test_four_six_brute_force():
+    """The {4,6} choice is the fp64 minimum of both candidates' squared errors."""
+    rng = np.random.default_rng(9)
+    close, n4 = 0, 0
+    for trial in range(4000):
+        x = (rng.standard_normal(16) * rng.choice([1, 1, 5, 30], 16)).astype(np.float32)
+        # per-tensor scale spread around amax/2688 so both E4M3 scales stay in range
+        g = float(np.float32(np.abs(x).max() / 2688 * np.exp(rng.uniform(0.5, 3.5))))
+        m, codes, sb, xh, e4, e6 = oracle.four_six_block(x, g)
+        c6, s6, x6 = oracle.nvfp4_block(x, 6, g)
+        c4, s4, x4 = oracle.nvfp4_block(x, 4, g)
+        d6 = float(np.sum((x.astype(np.float64) - x6) ** 2))
+        d4 = float(np.sum((x.astype(np.float64) - x4) ** 2))
+        assert s4 != s6
+        if abs(d4 - d6) <= 1e-5 * max(d4, d6):
+            close += 1
+            continue
+        want = 4 if d4 < d6 else 6
+        assert m == want
+        assert sb == (s4 if want == 4 else s6)
+        assert np.array_equal(codes, c4 if want == 4 else c6)
+        n4 += want == 4
+    assert close < 40
+    assert 200 < n4 < 3800     # both candidates are actually exercised
+
+
+def test_mx_block_brute_force():
+    rng = np.random.default_rng(10)
+    for trial in range(1500):
+        x = (rng.standard_normal(32) * np.exp(rng.uniform(-10, 10))).astype(np.float32)
+        e, codes, sb, xh, ea, eb = oracle.mx_block(x)
+        amax = float(np.max(np.abs(x)))
+        E = int(np.floor(np.log2(amax)))
+        assert 4 <= amax * 2.0 ** -(E - 2) < 8      # OCP shared-exponent candidate
+        assert e in (E - 2, E - 1) and sb == e + 127
+        sse = {}
+        for cand in (E - 2, E - 1):
+            v = (x * np.float32(2.0 ** -cand)).astype(np.float32)
+            cc = brute_e2m1(v)
+            rec = layout.E2M1[cc] * 2.0 ** cand
+            sse[cand] = float(np.sum((x.astype(np.float64) - rec) ** 2))
+            if cand == e:
+                assert np.array_equal(cc, codes)
+                assert np.array_equal(rec.astype(np.float32), xh)
+        other = (E - 1) if e == E - 2 else (E - 2)
+        if abs(sse[e] - sse[other]) > 1e-5 * max(sse.values()):
+            assert sse[e] < sse[other]
+
+
+# -------------------------------------------------------------- Hadamard ---
+
+def sylvester(n=128):
+    i = np.arange(n)
+    pc = np.vectorize(lambda a: bin(a).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+def test_fwht_is_sylvester_matrix():
+    H = sylvester()
+    eye = np.eye(128, dtype=np.float32)
+    cols = np.stack([oracle.fwht128(eye[j]) for j in range(128)], 1)
+    assert np.array_equal(cols.astype(np.float64), H)
+    assert np.array_equal(H @ H.T, 128 * np.eye(128))
+    rng = np.random.default_rng(11)
+    for _ in range(50):
+        x = rng.standard_normal(128).astype(np.float32)
+        y = oracle.fwht128(x).astype(np.float64)
+        ref = H @ x.astype(np.float64)
+        assert np.max(np.abs(y - ref)) <= 8 * 2 ** -24 * np.sum(np.abs(x)) + 1e-30
+
+
+def test_rotation_orthonormal_roundtrip():
+    r = np.float32(1 / np.sqrt(128))
+    assert r.view(np.uint32) == 0x3DB504F3
+    e0 = np.zeros(128, np.float32)
+    e0[0] = 1
+    assert np.all(oracle.rotate128(e0) == r)
+    rng = np.random.default_rng(12)
+    for _ in range(50):
+        x = rng.standard_normal(128).astype(np.float32)
+        y = oracle.rotate128(oracle.rotate128(x))
+        assert np.max(np.abs(y - x)) <= 16 * 2 ** -24 * 128 * np.max(np.abs(x))
+        assert abs(np.linalg.norm(oracle.rotate128(x)) - np.linalg.norm(x)) < 1e-5 * np.linalg.norm(x)
+
+
+# --------------------------------------------------------- memory ratio -----
+
+def test_memory_ratio_golden():
+    g = json.load(open(os.path.join(GOLDEN, "mem_ratio.json")))
+    f = lambda bits: 2.0 / (bits / 8.0 + 1.0 / g["block"])
+    assert abs(f(4) - g["ratio_4bit"]) < 1e-12 and abs(f(3) - g["ratio_3bit"]) < 1e-12
+    assert oracle.mem_ratio(oracle.make_config(fmt=oracle.FMT_NVFP4)) == pytest.approx(g["ratio_4bit"], abs=1e-12)
+    assert oracle.record_bytes(oracle.make_config(fmt=oracle.FMT_NVFP4)) == 9216
+    assert oracle.mem_ratio(oracle.make_config(fmt=oracle.FMT_MXFP4)) == pytest.approx(256 / 68, abs=1e-12)
+
+
+# ------------------------------------------------------- P quantization -----
+
+def test_p_block_tau_endpoints():
+    rng = np.random.default_rng(13)
+    for _ in range(300):
+        p = np.exp(-rng.exponential(3, 16))
+        if rng.random() < 0.5:
+            p = p * 1e-3
+        _, mode0 = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 8, 0.0)
+        _, mode448 = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 8, 448.0)
+        assert mode0 == 6 and mode448 == 2
+        a = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 1, 0.0)[0]
+        b = oracle.p_block(p, oracle.P_AMAX6, 8, 5.0)[0]
+        assert np.array_equal(a, b)
+        # the threshold compares the block's max of c*P against tau
+        u = np.float32(8 * p.max())
+        _, m_lo = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 8, float(np.nextafter(u, np.float32(0))))
+        _, m_hi = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 8, float(np.nextafter(u, np.float32(1e9))))
+        assert m_lo == 6 and m_hi == 2
+
+
+def test_p_block_closed_forms():
+    ones = np.ones(16)
+    ph, mode = oracle.p_block(ones, oracle.P_AMAX2_OR_AMAX6, 8, 1.0)
+    assert mode == 6 and np.all(ph == 1.03125)    # 8/6 -> E4M3 1.375; 8/1.375 -> 6; 6*1.375/8
+    ph, mode = oracle.p_block(ones, oracle.P_AMAX2_OR_AMAX6, 8, 448.0)
+    assert mode == 2 and np.all(ph == 1.0)
+    ph, _ = oracle.p_block(ones, oracle.P_AMAX6, 8, 0.0)
+    assert np.all(ph == 1.03125)
+    # underflow: with c = 1 tiny probabilities collapse, c = 8 keeps them
+    p = np.full(16, 1e-3)
+    p[0] = 2.5e-3
+    a = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 1, 0.0)[0]
+    b = oracle.p_block(p, oracle.P_AMAX2_OR_AMAX6, 8, 0.0)[0]
+    assert np.abs(b - p).max() <= np.abs(a - p).max()
+
+
+# -------------------------------------------------------------- query -------
+
+def test_query_exact_representable_has_zero_residual():
+    cfg = oracle.make_config(rotation=0, centering=0)
+    rng = np.random.default_rng(14)
+    grid = np.array([0, 0.21875, 0.4375, 0.65625, 0.875, 1.3125, 1.75, 2.625], np.float32)
+    q = (rng.choice(grid, (1, 32, 128)) * rng.choice([-1, 1], (1, 32, 128))).astype(np.float32)
+    q[..., ::16] = 2.625
+    qb = torch.from_numpy(q).to(torch.bfloat16).view(torch.uint16).numpy()
+    assert np.array_equal(torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).float().numpy(), q)
+    rec = oracle.quantize_query(cfg, qb, None)
+    qhat, g, qmu, codes, sb = layout.query_record(0, 32, rec[0])
+    assert g[0] == np.float32(2.0 ** -10) and g[1] == 1.0
+    assert not codes[1].any()
+    assert np.array_equal(qhat, q[0].astype(np.float64))
+
+
+def test_query_residual_reduces_error():
+    rng = np.random.default_rng(15)
+    for fmt in (0, 1):
+        for rot in (0, 1):
+            cfg = oracle.make_config(fmt=fmt, rotation=rot, centering=0)
+            cfg1 = oracle.make_config(fmt=fmt, rotation=rot, centering=0, query_terms=1)
+            q = torch.randn(3, 32, 128, generator=torch.Generator().manual_seed(fmt * 2 + rot)).to(torch.bfloat16)
+            qb = q.view(torch.uint16).numpy()
+            ref = q.float().numpy().astype(np.float64)
+            if rot:
+                ref = ref @ (sylvester() / np.sqrt(128))
+            two = oracle.quantize_query(cfg, qb, None)
+            one = oracle.quantize_query(cfg1, qb, None)
+            for b in range(3):
+                q2 = layout.query_record(fmt, 32, two[b])[0]
+                q1 = layout.query_record(fmt, 32, one[b])[0]
+                e1 = np.linalg.norm(ref[b] - q1)
+                e2 = np.linalg.norm(ref[b] - q2)
+                assert e2 < 0.35 * e1
+                assert np.array_equal(one[b][:32 * 64], two[b][:32 * 64])   # term 1 is shared
+
+
+def test_query_qmu():
+    cfg = oracle.make_config()
+    mu = np.random.default_rng(16).standard_normal((8, 128)).astype(np.float32)
+    q = torch.randn(2, 32, 128, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    rec = oracle.quantize_query(cfg, q.view(torch.uint16).numpy(), mu)
+    for b in range(2):
+        qmu = layout.query_record(0, 32, rec[b])[2]
+        ref = np.einsum("jd,jd->j", q[b].double().numpy(), np.repeat(mu, 4, 0).astype(np.float64))
+        assert np.allclose(qmu, ref, rtol=1e-6, atol=1e-6)
+
+
+# --------------------------------------------------------------- writer -----
+
+def make_pages(n, seed, H=8):
+    from nvfp4_kv_cache_bd_gb300 import synth
+    mu, mask = synth.key_mean(H, seed)
+    k, v = synth.keys_values(n * 128, H, seed, mu=mu, mask=mask)
+    return k.view(n, 128, H, 128), v.view(n, 128, H, 128), mu
+
+
+@pytest.mark.parametrize("fmt,rot,cen,ks", [(0, 1, 1, 1), (0, 0, 0, 0), (1, 1, 1, 1), (0, 1, 0, 1)])
+def test_writer_reconstruction(fmt, rot, cen, ks):
+    from nvfp4_kv_cache_bd_gb300 import synth
+    cfg = oracle.make_config(fmt=fmt, rotation=rot, centering=cen, key_search=ks)
+    k, v, mu = make_pages(2, 21)
+    gk, gv = synth.gscales(k.reshape(-1, 8, 128), v.reshape(-1, 8, 128), mu, bool(rot), bool(cen))
+    pool = np.zeros(4 * 8 * 2 * oracle.record_bytes(cfg), np.uint8)
+    dst = np.array([3, 1], np.int32)
+    oracle.quantize_kv_pages(cfg, k.view(torch.uint16).numpy(), v.view(torch.uint16).numpy(), dst,
+                             mu.numpy(), gk, gv, pool)
+    H128 = sylvester() / np.sqrt(128)
+    for i, page in enumerate(dst):
+        for h in range(8):
+            x = k[i, :, h].double().numpy()
+            if cen:
+                x = x - mu[h].double().numpy()
+            if rot:
+                x = x @ H128
+            _, ksb, kval = layout.k_record(fmt, layout.pool_record(pool, fmt, 8, page, h, 0))
+            _, vsb, vval = layout.v_record(fmt, layout.pool_record(pool, fmt, 8, page, h, 1))
+            gK = gk if fmt == 0 else 1.0
+            gV = gv if fmt == 0 else 1.0
+            kb = 16 if fmt == 0 else 32
+            Sk = np.repeat(layout.scale_values(fmt, ksb), kb, 1) * gK
+            Sv = np.repeat(layout.scale_values(fmt, vsb), kb, 1) * gV
+            # largest grid gap (4 -> 6) bounds NVFP4 errors by S; the MX e0 candidate may
+            # saturate amax/2^e in [6, 8) down to 6, an error below 2 S
+            bound = 1.0 if fmt == 0 else 2.0
+            assert np.all(np.abs(kval * gK - x) <= bound * Sk * (1 + 1e-5) + 1e-6)
+            assert np.all(np.abs(vval * gV - v[i, :, h].double().numpy()) <= bound * Sv * (1 + 1e-5) + 1e-6)
+            rel = np.linalg.norm(kval * gK - x) / np.linalg.norm(x)
+            assert rel < 0.12
+    # untouched pages stay zero
+    rb = oracle.record_bytes(cfg)
+    assert not pool[0:8 * 2 * rb].any() and not pool[2 * 8 * 2 * rb:3 * 8 * 2 * rb].any()
+
+
+def test_writer_four_six_helps_keys():
+    """Keys quantized with the {4,6} search have lower error than amax6 alone."""
+    from nvfp4_kv_cache_bd_gb300 import synth
+    k, v, mu = make_pages(1, 22)
+    errs = {}
+    for ks in (0, 1):
+        cfg = oracle.make_config(key_search=ks)
+        gk, gv = synth.gscales(k.reshape(-1, 8, 128), v.reshape(-1, 8, 128), mu, True, True)
+        pool = np.zeros(8 * 2 * oracle.record_bytes(cfg), np.uint8)
+        oracle.quantize_kv_pages(cfg, k.view(torch.uint16).numpy(), v.view(torch.uint16).numpy(),
+                                 np.array([0], np.int32), mu.numpy(), gk, gv, pool)
+        x = (k[0].double() - mu.double().unsqueeze(0)).numpy() @ (sylvester() / np.sqrt(128))
+        e = 0.0
+        for h in range(8):
+            kval = layout.k_record(0, layout.pool_record(pool, 0, 8, 0, h, 0))[2] * gk
+            e += np.sum((kval - x[:, h]) ** 2)
+        errs[ks] = e
+    assert errs[1] < 0.97 * errs[0]
+
+
+# ------------------------------------------------------------ attention -----
+
+def sdpa_fp64(q, k, v):
+    """q [Hq][D], k/v [L][Hkv][D] (torch) -> [Hq][D] fp64 via the library routine."""
+    Hq, H = q.shape[0], k.shape[1]
+    kk = k.double().permute(1, 0, 2).repeat_interleave(Hq // H, 0)
+    vv = v.double().permute(1, 0, 2).repeat_interleave(Hq // H, 0)
+    out = torch.nn.functional.scaled_dot_product_attention(q.double().unsqueeze(1), kk, vv)
+    return out.squeeze(1).numpy()
+
+
+def build_case(L, seed, cfg, B=1, shuffle=True):
+    """Seeded hybrid-cache inputs for B sequences of length L (oracle side)."""
+    from nvfp4_kv_cache_bd_gb300 import synth
+    H, Hq = cfg.num_kv_heads, cfg.num_q_heads
+    mu, mask = synth.key_mean(H, seed)
+    ks, vs = [], []
+    for b in range(B):
+        k, v = synth.keys_values(L, H, seed * 100 + b, mu=mu, mask=mask)
+        ks.append(k)
+        vs.append(v)
+    q = synth.query(B, Hq, seed)
+    ns, npg, nt = synth.split_tokens(L)
+    gk, gv = synth.gscales(torch.cat(ks), torch.cat(vs), mu, bool(cfg.rotation), bool(cfg.centering))
+    nphys = max(1, B * npg)
+    perm = synth.page_permutation(nphys, seed).numpy() if shuffle else np.arange(nphys, dtype=np.int32)
+    bt = np.zeros((B, max(1, npg)), np.int32)
+    pool = np.zeros(nphys * H * 2 * oracle.record_bytes(cfg), np.uint8)
+    sink_k = torch.zeros(B, 16, H, 128, dtype=torch.bfloat16)
+    sink_v = torch.zeros_like(sink_k)
+    tail_k = torch.zeros(B, 128, H, 128, dtype=torch.bfloat16)
+    tail_v = torch.zeros_like(tail_k)
+    for b in range(B):
+        k, v = ks[b], vs[b]
+        sink_k[b, :ns] = k[:ns]
+        sink_v[b, :ns] = v[:ns]
+        bt[b, :npg] = perm[b * npg:(b + 1) * npg]
+        if npg:
+            kp = k[16:16 + 128 * npg].reshape(npg, 128, H, 128)
+            vp = v[16:16 + 128 * npg].reshape(npg, 128, H, 128)
+            oracle.quantize_kv_pages(cfg, kp.view(torch.uint16).numpy(), vp.view(torch.uint16).numpy(),
+                                     bt[b, :npg], mu.numpy(), gk, gv, pool)
+        tail_k[b, :nt] = k[16 + 128 * npg:]
+        tail_v[b, :nt] = v[16 + 128 * npg:]
+    qp = oracle.quantize_query(cfg, q.view(torch.uint16).numpy(), mu.numpy())
+    u16 = lambda t: t.view(torch.uint16).numpy()
+    return dict(q=q, k=ks, v=vs, mu=mu, gk=gk, gv=gv, pool=pool, bt=bt, seq_lens=np.full(B, L, np.int32),
+                sink_k=u16(sink_k), sink_v=u16(sink_v), tail_k=u16(tail_k), tail_v=u16(tail_v), qp=qp)
+
+
+def run_oracle(cfg, c, tau=1.0, flags=0):
+    return oracle.decode_attention(cfg, c["qp"], c["q"].view(torch.uint16).numpy(), c["mu"].numpy(), c["pool"],
+                                   c["bt"], c["seq_lens"], c["sink_k"], c["sink_v"], c["tail_k"], c["tail_v"],
+                                   tau, c["gk"], c["gv"], flags)
+
+
+@pytest.mark.parametrize("L", [1, 5, 16, 17, 100, 143])
+def test_bf16_only_contexts_are_textbook_attention(L):
+    cfg = oracle.make_config()
+    c = build_case(L, 31, cfg)
+    out = run_oracle(cfg, c)
+    ref = sdpa_fp64(c["q"][0], c["k"][0], c["v"][0])
+    assert np.max(np.abs(out[0] - ref)) < 1e-12
+
+
+@pytest.mark.parametrize("fmt,rot,cen", [(0, 1, 1), (1, 1, 1), (0, 0, 0), (1, 0, 1)])
+def test_exact_p_equals_softmax_over_dequantized_operands(fmt, rot, cen):
+    """With P unquantized the segmented merge is one softmax over all tokens:
+    FP4 logits sm*(Qhat.Khat*gK + q.mu), BF16 logits sm*q.k (layout read by
+    the test's own decoder)."""
+    cfg = oracle.make_config(fmt=fmt, rotation=rot, centering=cen, p_mode=oracle.P_NONE)
+    L = 16 + 3 * 128 + 37
+    c = build_case(L, 32, cfg, B=2)
+    out = run_oracle(cfg, c)
+    sm = 1 / np.sqrt(128)
+    gK = c["gk"] if fmt == 0 else 1.0
+    gV = c["gv"] if fmt == 0 else 1.0
+    for b in range(2):
+        qhat = layout.query_record(fmt, 32, c["qp"][b])[0]
+        q = c["q"][b].double().numpy()
+        k = c["k"][b].double().numpy()
+        v = c["v"][b].double().numpy()
+        for j in range(32):
+            h = j // 4
+            logits, vals = [], []
+            for t in range(16):
+                logits.append(sm * q[j] @ k[t, h])
+                vals.append(v[t, h])
+            for p in range(3):
+                _, _, kv = layout.k_record(fmt, layout.pool_record(c["pool"], fmt, 8, c["bt"][b, p], h, 0))
+                _, _, vv = layout.v_record(fmt, layout.pool_record(c["pool"], fmt, 8, c["bt"][b, p], h, 1))
+                qmu = q[j] @ c["mu"][h].double().numpy() if cen else 0.0
+                logits += list(sm * (kv @ qhat[j] * gK + qmu))
+                vals += list(vv * gV)
+            for t in range(16 + 3 * 128, L):
+                logits.append(sm * q[j] @ k[t, h])
+                vals.append(v[t, h])
+            logits = np.array(logits)
+            w = np.exp(logits - logits.max())
+            ref = (w[:, None] * np.array(vals)).sum(0) / w.sum()
+            assert np.max(np.abs(out[b, j] - ref)) < 1e-12
+
+
+@pytest.mark.parametrize("rot,cen", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_identity_quantizers_transforms_cancel(rot, cen):
+    cfg = oracle.make_config(rotation=rot, centering=cen)
+    from nvfp4_kv_cache_bd_gb300 import synth
+    mu, mask = synth.key_mean(8, 41)
+    k, v = synth.keys_values(300, 8, 41, mu=mu, mask=mask)
+    q = synth.query(1, 32, 41)[0]
+    out = oracle.attention_identity_quant(cfg, q.view(torch.uint16).numpy(), k.view(torch.uint16).numpy(),
+                                          v.view(torch.uint16).numpy(), mu.numpy())
+    ref = sdpa_fp64(q, k, v)
+    assert np.max(np.abs(out - ref)) < 2e-5
+
+
+@pytest.mark.parametrize("tau,c,pmode,flags,factor", [
+    (1.0, 8, oracle.P_AMAX2_OR_AMAX6, 0, 1.03125),
+    (448.0, 8, oracle.P_AMAX2_OR_AMAX6, 0, 1.0),
+    (0.0, 8, oracle.P_AMAX6, 0, 1.03125),
+    (1.0, 8, oracle.P_AMAX2_OR_AMAX6, oracle.FLAG_QUANT_DENOM, None),
+])
+def test_equal_keys_closed_form(tau, c, pmode, flags, factor):
+    """All keys equal: every page has uniform P = 1, so Phat is one constant."""
+    cfg = oracle.make_config(p_mode=pmode, p_c=c)
+    n = 3
+    L = 16 + 128 * n
+    case = build_case(L, 51, cfg)
+    k1 = torch.from_numpy(case["sink_k"]).view(torch.bfloat16)[0, 0].clone()   # token 0's keys
+    kall = k1.unsqueeze(0).repeat(L, 1, 1)
+    case["k"] = [kall]
+    sink_k = torch.zeros(1, 16, 8, 128, dtype=torch.bfloat16)
+    sink_k[0] = kall[:16]
+    case["sink_k"] = sink_k.view(torch.uint16).numpy()
+    kp = kall[16:].reshape(n, 128, 8, 128)
+    vp = case["v"][0][16:].reshape(n, 128, 8, 128)
+    case["pool"][:] = 0
+    oracle.quantize_kv_pages(cfg, kp.view(torch.uint16).numpy(), vp.view(torch.uint16).numpy(), case["bt"][0],
+                             case["mu"].numpy(), case["gk"], case["gv"], case["pool"])
+    out = run_oracle(cfg, case, tau=tau, flags=flags)
+    # the FP4 logits differ from the BF16 ones by quantization, so isolate the pages:
+    # compare each q head against the closed form with the segment weights written out
+    sm = 1 / np.sqrt(128)
+    q = case["q"][0].double().numpy()
+    qhat = layout.query_record(0, 32, case["qp"][0])[0]
+    v = case["v"][0].double().numpy()
+    for j in range(32):
+        h = j // 4
+        s_bf = sm * q[j] @ kall[0, h].double().numpy()
+        kv = layout.k_record(0, layout.pool_record(case["pool"], 0, 8, case["bt"][0, 0], h, 0))[2]
+        s_fp = sm * (kv[0] @ qhat[j] * case["gk"] + q[j] @ case["mu"][h].double().numpy())
+        M = max(s_bf, s_fp)
+        wb, wf = np.exp(s_bf - M), np.exp(s_fp - M)
+        vhat = np.concatenate([layout.v_record(0, layout.pool_record(case["pool"], 0, 8, case["bt"][0, p], h, 1))[2]
+                               for p in range(n)]) * case["gv"]
+        f = factor if factor is not None else 1.03125
+        num = wb * v[:16, h].sum(0) + wf * f * vhat.sum(0)
+        den = wb * 16 + wf * (128 * n if factor is not None else f * 128 * n)
+        assert np.max(np.abs(out[0, j] - num / den)) < 1e-12
+
+
+def test_softmax_rows_sum_to_one_before_quantization():
+    """V = 1.5 everywhere (exact in NVFP4 with g_V = 0.25): any normalisation
+    slip shows up as an output != 1.5."""
+    cfg = oracle.make_config(p_mode=oracle.P_NONE)
+    L = 16 + 2 * 128 + 50
+    c = build_case(L, 61, cfg)
+    const = lambda *shape: torch.full(shape, 1.5, dtype=torch.bfloat16).view(torch.uint16).numpy()
+    c["sink_v"], c["tail_v"] = const(1, 16, 8, 128), const(1, 128, 8, 128)
+    kp = c["k"][0][16:16 + 256].reshape(2, 128, 8, 128)
+    c["gv"] = 0.25
+    oracle.quantize_kv_pages(cfg, kp.view(torch.uint16).numpy(), const(2, 128, 8, 128), c["bt"][0],
+                             c["mu"].numpy(), c["gk"], c["gv"], c["pool"])
+    out = run_oracle(cfg, c)
+    assert np.max(np.abs(out - 1.5)) < 1e-12
+
+
+def test_empty_sequence_gives_zero():
+    cfg = oracle.make_config()
+    c = build_case(40, 71, cfg)
+    c["seq_lens"] = np.zeros(1, np.int32)
+    assert not run_oracle(cfg, c).any()
