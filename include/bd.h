@@ -1,0 +1,211 @@
+/*
+ * bd.h -- C ABI of the GB300 (sm_103a) NVFP4 KV-cache hot path:
+ *   - the page-fill writer that quantizes freshly filled 128-token KV pages,
+ *   - the two-term FP4 query quantizer,
+ *   - paged single-token decode attention that reads the packed FP4 K/V.
+ *
+ * Method sources (cited by page title and section):
+ *  [cfg]  BitDecoding-FP4 "evaluation/config.py": RECIPE (key smoothing,
+ *         Hadamard rotation, adaptive {4,6} block-scale search, dual residual
+ *         query quantization, underflow-aware probability scaling),
+ *         recipe_additional_config, probability_environment, KV_MODES
+ *         ("bitdecoding-nvfp4": 16-token BF16 sink, key_scale_geometry
+ *         "local"; "bitdecoding-mxfp4": scale_mode "mxfp4_search"),
+ *         PARITY_ENGINE_KWARGS (block_size 128).
+ *  [ab]   kv-landlords "scripts/quant_ab.py": module docstring (each page is
+ *         quantized once when it fills; the partial hot page stays BF16),
+ *         mem_ratio (4-bit codes plus one 1-byte scale per 16 elements).
+ *  [arch] "How openbitsys/bitdecoding-fp4 works": KV cache writer ->
+ *         KV quantization ("quantizes pages"), decode interface -> paged
+ *         attention kernel, hybrid cache.
+ *
+ * Conventions shared by every call:
+ *  - Every call returns an int status (BD_OK or a negative BD_ERR_*); no C++
+ *    exception crosses this boundary.  Argument errors are detected on the
+ *    host before anything is launched and leave device memory untouched.
+ *  - All tensors are caller-owned device memory unless a parameter says
+ *    "host".  The library owns only the bd_ctx, its per-layer key-shift copy
+ *    and its device error word.
+ *  - Launch calls take a cudaStream_t as void*, are asynchronous and never
+ *    synchronize.  Device-side failures (a bounded wait that ran out) are
+ *    recorded in the context's device error word; read it with
+ *    bd_read_device_error().
+ *  - bf16 tensors are raw 16-bit bfloat16 bit patterns (const void*).
+ *  - The first launch call on a device allocates the context's device state
+ *    (key-shift table, error word) with cudaMalloc; make that first call, or
+ *    bd_set_key_shift(), before capturing a stream into a CUDA graph.
+ *
+ * ---------------------------------------------------------------------------
+ * Byte layouts (both the CUDA path and the independent CPU oracle write these)
+ * ---------------------------------------------------------------------------
+ *  E2M1 code: bit 3 = sign, bits 2..0 index {0, .5, 1, 1.5, 2, 3, 4, 6}.
+ *  NVFP4 block: 16 consecutive head-dim elements share one E4M3 (FN) scale
+ *    byte; the tensor also has one fp32 per-tensor scale g (k_gscale /
+ *    v_gscale, or the query's own g1/g2).  value = E2M1 * E4M3 * g.
+ *  MXFP4 block: 32 consecutive head-dim elements share one UE8M0 byte
+ *    (value 2^(byte-127)); no per-tensor scale.  value = E2M1 * 2^(byte-127).
+ *
+ *  KV pool of one layer: records ordered [physical page][kv head][K, V].
+ *    record bytes R = 8192 + 128*nb, nb = 8 (NVFP4) or 4 (MXFP4):
+ *    R = 9216 (NVFP4), 8704 (MXFP4).  bd_record_bytes() returns R.
+ *    The K record:
+ *      codes [128 tokens][64 B]: element d of a token's head vector is in
+ *        byte d/2, even d in the low nibble.  Elements are in the rotated,
+ *        centered domain when rotation / centering are on.
+ *      scales[128 tokens][nb]: scale byte of block b of that token.
+ *    The V record pairs token tau = 16 i + p with token tau + 8
+ *    (16-token group i = 0..7, p = 0..7):
+ *      codes [8 i][8 p][128 d]: byte = code(tau, d) | code(tau + 8, d) << 4.
+ *      scales[8 i][8 p][nb][2]: scale bytes of block b, token tau first.
+ *    FP4 page p of a sequence holds its tokens 16 + 128 p ... 16 + 128 p + 127
+ *    (tokens 0..15 are the BF16 sink).
+ *
+ *  Packed query of one token (stride bd_query_packed_bytes(), a multiple of
+ *  256): for Hq query heads and terms t = 0, 1:
+ *      codes  at (t*Hq + j)*64                 [64 B] (same nibble order as K)
+ *      scales at 2*Hq*64 + (t*Hq + j)*nb       [nb B]
+ *      g      at 2*Hq*64 + 2*Hq*8              float[2] (g1, g2; MXFP4: 1, 1)
+ *      q.mu   at 2*Hq*64 + 2*Hq*8 + 16         float[Hq] (unrotated bf16 q
+ *                                              times the layer's key mean)
+ *    all other bytes zero.  With query_terms = 1 the second term's codes and
+ *    scales are zero and g2 = 0.
+ */
+#ifndef BD_H
+#define BD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    BD_OK = 0,
+    BD_ERR_INVALID_ARG = -1,  /* null pointer, size out of range, non-finite or out-of-range scalar */
+    BD_ERR_UNSUPPORTED = -2,  /* a configuration this build does not implement */
+    BD_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+    BD_ERR_WORKSPACE = -4,    /* the caller's workspace is smaller than required */
+    BD_ERR_TIMEOUT = -5       /* a bounded device-side wait ran out (reported via the error word) */
+};
+
+enum { BD_FORMAT_NVFP4 = 0, BD_FORMAT_MXFP4 = 1 };
+
+/* Probability quantization modes ([cfg] probability_environment):
+ * BD_P_AMAX6 is the mode used when underflow-aware scaling is disabled;
+ * BD_P_AMAX2_OR_AMAX6 is "amax2_or_amax6" (p_c = 1) or "..._c8" (p_c = 8);
+ * BD_P_NONE keeps probabilities unquantized (ablation). */
+enum { BD_P_NONE = 0, BD_P_AMAX6 = 1, BD_P_AMAX2_OR_AMAX6 = 2 };
+
+typedef struct bd_config {
+    int num_layers;    /* >= 1: number of key-shift tables held by the context */
+    int num_q_heads;   /* must equal 4 * num_kv_heads (GQA group of 4) */
+    int num_kv_heads;  /* 1..16 */
+    int head_dim;      /* must be 128 */
+    int page_size;     /* must be 128 ([cfg] PARITY_ENGINE_KWARGS block_size) */
+    int sink_tokens;   /* must be 16 ([cfg] KV_MODES sink_tokens) */
+    int format;        /* BD_FORMAT_NVFP4 or BD_FORMAT_MXFP4 */
+    int key_search;    /* NVFP4 keys: 1 = adaptive {4,6} search ("four_six"), 0 = "amax6" */
+    int rotation;      /* 1 = Hadamard rotation of K and Q along head_dim ("hadamard"), 0 = "none" */
+    int centering;     /* 1 = key smoothing: subtract the static per-channel key mean */
+    int query_terms;   /* 2 = dual residual query (Q ~ Q1 + Q2), 1 = single term */
+    int p_mode;        /* BD_P_* */
+    int p_c;           /* 1 or 8 ([cfg] probability_environment: "supports c=1 or c=8") */
+} bd_config;
+
+typedef struct bd_ctx bd_ctx;
+
+/* Validate cfg and create a context (host memory only; no CUDA call).
+ * Returns BD_ERR_INVALID_ARG for null pointers or values out of range,
+ * BD_ERR_UNSUPPORTED for head_dim / page_size / sink / GQA ratios this build
+ * does not implement.  *out is set only on success. */
+int bd_create(const bd_config* cfg, bd_ctx** out);
+
+/* Free the context and its device state (safe on NULL). */
+void bd_destroy(bd_ctx* ctx);
+
+/* Static text for a status code. */
+const char* bd_status_string(int status);
+
+/* Copy one layer's static key mean mu [num_kv_heads][128] fp32 from HOST
+ * memory into the context ([cfg] RECIPE key_smoothing; KEY_SHIFT_SIDECAR holds
+ * these means).  The default mean of every layer is zero.  Synchronous. */
+int bd_set_key_shift(bd_ctx* ctx, int layer, const float* mu_host);
+
+/* Bytes of one pool record (9216 NVFP4, 8704 MXFP4); a layer's pool holds
+ * pages * num_kv_heads * 2 records. */
+size_t bd_record_bytes(const bd_ctx* ctx);
+
+/* Bytes of one packed query token (a multiple of 256). */
+size_t bd_query_packed_bytes(const bd_ctx* ctx);
+
+/* Page-fill writer ([ab] freeze-at-fill; [arch] KV cache writer -> KV
+ * quantization).  Quantizes n freshly filled pages of one layer, K and V in
+ * one launch:
+ *   k, v      : bf16 [n][128 tokens][num_kv_heads][128], device, read only.
+ *   dst_pages : int32 [n], device: physical page of each input page in kv_pool.
+ *   K = rotate(bf16 - mu[layer]) (per config), then per 16-element block the
+ *   {4,6} search (or amax6) with per-tensor scale k_gscale; NVFP4 V uses
+ *   amax6 with v_gscale; MXFP4 uses the mxfp4 search for both and ignores the
+ *   g scales.  The records of the given pages are overwritten; nothing else
+ *   in kv_pool is touched.  g scales must be finite and in [1e-30, 1e30].
+ *   n = 0 is a no-op.  Destination pages must be distinct. */
+int bd_quantize_kv_pages(bd_ctx* ctx, int layer, const void* k, const void* v,
+                         const int32_t* dst_pages, int n, float k_gscale, float v_gscale,
+                         void* kv_pool, void* stream);
+
+/* Two-term query quantization ([cfg] RECIPE dual_residual_query_quantization,
+ * query scale mode "amax6"): per token, q -> rotate -> Q1 with g1 =
+ * amax/2688 over the token's num_q_heads*128 values -> residual R = q_rot -
+ * Q1hat -> Q2 with g2 = amax(R)/2688 (a zero amax gives g = 1).
+ *   q        : bf16 [B][num_q_heads][128], device.
+ *   q_packed : B * bd_query_packed_bytes() bytes, device, written entirely.
+ *   B = 0 is a no-op. */
+int bd_quantize_query(bd_ctx* ctx, int layer, const void* q, int B, void* q_packed, void* stream);
+
+/* Workspace bytes bd_decode_attention needs for B sequences whose block
+ * table rows hold max_blocks entries (0 if B == 0). */
+size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
+
+/* Paged single-token decode attention over the hybrid cache ([arch] decode
+ * interface -> paged attention kernel; [cfg] sink_tokens, block_size):
+ *   q_packed    : from bd_quantize_query, device.
+ *   q           : bf16 [B][num_q_heads][128], device (raw query, used by the
+ *                 BF16 sink and tail tokens).
+ *   kv_pool     : the layer's pool (layout above), device.
+ *   block_table : int32 [B][max_blocks], device: physical page of each FP4
+ *                 page of each sequence.
+ *   seq_lens    : int32 [B], device: context length L of each sequence
+ *                 (0 <= L <= 16 + 128*max_blocks + 127); L = 0 gives zeros.
+ *   sink_k/v    : bf16 [B][16][num_kv_heads][128]: tokens 0..min(L,16)-1.
+ *   tail_k/v    : bf16 [B][128][num_kv_heads][128]: the partial page, tokens
+ *                 16 + 128*npages ... L-1 in rows 0.., npages = max(0,L-16) div 128.
+ *   tau         : probability threshold, finite, in [0, 448]
+ *                 ([cfg] probability_environment).
+ *   k/v_gscale  : the per-tensor scales the layer's pages were written with.
+ *   out         : fp32 [B][num_q_heads][128], device.
+ *   ws          : device scratch of at least bd_decode_workspace_size(ctx, B,
+ *                 max_blocks) bytes; its contents need no initialisation.
+ * Query head j reads kv head j / 4; softmax scale 1/sqrt(128). */
+int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q,
+                        const void* kv_pool, const int32_t* block_table, int max_blocks,
+                        const int32_t* seq_lens, const void* sink_k, const void* sink_v,
+                        const void* tail_k, const void* tail_v, int B, float tau,
+                        float k_gscale, float v_gscale, float* out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Synchronize `stream`, copy the context's device error word into *out
+ * (BD_OK or BD_ERR_TIMEOUT) and reset it to BD_OK. */
+int bd_read_device_error(bd_ctx* ctx, void* stream, int* out);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier phase nothing will complete, for at most timeout_us microseconds
+ * (1..2000000), then records BD_ERR_TIMEOUT in the device error word and
+ * returns.  Read the result with bd_read_device_error(). */
+int bd_selftest_bounded_wait(bd_ctx* ctx, int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BD_H */

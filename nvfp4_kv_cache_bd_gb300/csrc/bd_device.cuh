@@ -1,0 +1,169 @@
+// Device helpers for the sm_103a kernels: FP4/FP8 conversions through the
+// hardware cvt instructions, exact IEEE arithmetic without contraction,
+// mbarrier + bulk-copy (TMA) primitives with bounded waits, and the
+// m16n8k16 f16 tensor-core MMA.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "bd_internal.h"
+
+namespace bd {
+
+constexpr float kRot = 0.08838834764831845f;   // binary32(1/sqrt(128)) = 0x3DB504F3
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- formats --
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two binary32 values -> one byte of two E2M1 codes (lo in bits 3..0, hi in
+// bits 7..4); round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One byte of two E2M1 codes -> f16x2 (low nibble -> low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t r;
+    uint16_t b = (uint16_t)byte;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "h"(b));
+    return r;
+}
+
+// Binary32 -> E4M3 byte, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3(float s) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+    return r & 0xFFu;
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    uint32_t r;
+    uint16_t b = (uint16_t)two;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(b));
+    return r;
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t byte) {
+    uint32_t h = e4m3x2_to_f16x2(byte & 0xFFu);
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
+    return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+// 2^e for e in [-127, 127], exact (2^-127 is subnormal).
+__device__ __forceinline__ float pow2i(int e) {
+    return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// floor(log2 a) for a finite a > 0 read from its exponent field.
+__device__ __forceinline__ int ilog2f(float a) {
+    uint32_t u = __float_as_uint(a);
+    int e = (int)((u >> 23) & 0xFF);
+    if (e != 0) return e - 127;
+    return (31 - __clz((int)(u & 0x7FFFFF))) - 149;
+}
+
+// ------------------------------------------------------------- f16x2 math --
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bcast_lo(uint32_t h) { return (h & 0xFFFFu) | (h << 16); }
+__device__ __forceinline__ uint32_t bcast_hi(uint32_t h) { return (h >> 16) | (h & 0xFFFF0000u); }
+
+// D += A(16x16, row) * B(16x8, col), f16 inputs, f32 accumulate.
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------ mbarrier and TMA --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// limit_ns nanoseconds, giving up early when *abort_flag becomes nonzero.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  const volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// Bulk asynchronous copy global -> shared (TMA unit), completing `bytes`
+// transaction bytes on the mbarrier.  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+}  // namespace bd

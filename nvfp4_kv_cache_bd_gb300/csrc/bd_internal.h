@@ -1,0 +1,67 @@
+// Internal declarations shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/bd.h"
+
+namespace bd {
+
+constexpr int kD = 128;          // head_dim
+constexpr int kPage = 128;       // tokens per FP4 page
+constexpr int kSink = 16;        // BF16 sink tokens
+constexpr int kGroup = 4;        // query heads per kv head
+constexpr int kCodeBytes = 8192; // codes of one record
+constexpr int kPartStride = 132; // floats per split partial: m, l, pad, pad, O[128]
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
+
+__host__ __device__ inline int nblocks(int format) { return format == BD_FORMAT_NVFP4 ? 8 : 4; }
+__host__ __device__ inline int record_bytes(int format) { return kCodeBytes + kPage * nblocks(format); }
+inline size_t qpack_stride(int hq) { return ((size_t)hq * (2 * 64 + 2 * 8 + 4) + 16 + 255) / 256 * 256; }
+
+struct WriterArgs {
+    const uint16_t* k;
+    const uint16_t* v;
+    const int32_t* dst_pages;
+    const float* mu;          // [Hkv][128] of this layer (device)
+    uint8_t* pool;
+    int n, hkv, format, key_search, rotation, centering;
+    float gk, gv;
+};
+
+struct QueryArgs {
+    const uint16_t* q;
+    const float* mu;          // [Hkv][128] of this layer (device)
+    uint8_t* qp;
+    int B, hq, format, rotation, centering, terms;
+    size_t stride;
+};
+
+struct DecodeArgs {
+    const uint8_t* qp;
+    const uint16_t* q;
+    const uint8_t* pool;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const uint16_t* sink_k;
+    const uint16_t* sink_v;
+    const uint16_t* tail_k;
+    const uint16_t* tail_v;
+    float* out;
+    float* ws;                // [B][Hq][nsplit + 1][kPartStride]
+    int* err;
+    size_t qstride;
+    int B, hq, hkv, max_blocks, nsplit, pages_per_split;
+    int format, centering, p_mode, p_c;
+    float tau, gk, gv;
+};
+
+cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s);
+cudaError_t launch_query(const QueryArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);
+void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split);
+
+}  // namespace bd

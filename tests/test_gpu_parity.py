@@ -1,0 +1,159 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Bars: packed K/V records and packed query bytes bit-exact (the fp32 q.mu
+field within 1e-5 relative); attention outputs within max-abs 2e-3 and
+relative-L2 1e-3 of the oracle's fp64 attention on the same quantized
+operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_kv_cache_bd_gb300 as bd
+from tests import cases
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, REL_L2 = 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from nvfp4_kv_cache_bd_gb300 import build
+    build.build_library()
+    build.build_oracle()
+
+
+def check(spec: cases.Spec, attn=True):
+    c = cases.build(spec)
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c, pool_only=not attn)
+    diff = np.nonzero(gpu["pool"] != ora["pool"])[0]
+    assert diff.size == 0, f"{diff.size} pool bytes differ, first at {diff[:8]}"
+    assert np.array_equal(cases.strip_qmu(c, gpu["qp"]), cases.strip_qmu(c, ora["qp"]))
+    np.testing.assert_allclose(cases.qmu_of(c, gpu["qp"]), cases.qmu_of(c, ora["qp"]), rtol=1e-5, atol=1e-4)
+    assert gpu["bf16_unchanged"]
+    if attn:
+        mx, rl = cases.attn_errors(gpu["out"], ora["out"])
+        assert mx < MAX_ABS and rl < REL_L2, (mx, rl)
+    assert bd.read_device_error(c.ctx) == bd.OK
+    return c, gpu, ora
+
+
+def test_single_sequence_4k_full_recipe():
+    """One layer, 32 q / 8 kv heads, context 4096: 16 sink + 31 pages + 112 tail."""
+    check(cases.Spec(lens=[4096], seed=0, tau=1.0))
+
+
+def test_ragged_batch_edge_lengths():
+    lens = [1, 5, 16, 17, 143, 144, 16 + 128 * 2 + 1, 16 + 128 * 3 + 127, 16 + 128 * 9]
+    check(cases.Spec(lens=lens, seed=3))
+
+
+@pytest.mark.parametrize("tau", [0.0, 0.5, 4.0, 448.0])
+def test_tau_sweep(tau):
+    check(cases.Spec(lens=[16 + 128 * 6 + 50, 900], seed=11, tau=tau))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(p_mode=bd.P_AMAX6),
+    dict(p_mode=bd.P_NONE),
+    dict(p_c=1, tau=0.5),
+    dict(rotation=0, centering=0, key_search=0, terms=1),
+    dict(rotation=1, centering=0),
+    dict(rotation=0, centering=1),
+    dict(terms=1),
+    dict(key_search=0),
+])
+def test_recipe_switches(kw):
+    check(cases.Spec(lens=[16 + 128 * 5 + 77, 300], seed=21, **kw))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(rotation=0, centering=0), dict(terms=1)])
+def test_mxfp4(kw):
+    check(cases.Spec(lens=[16 + 128 * 7 + 3, 16 + 128 * 2 + 100], seed=31, fmt=1, **kw))
+
+
+def test_unshuffled_and_single_page():
+    check(cases.Spec(lens=[16 + 128], seed=41, shuffle=False))
+
+
+def test_writer_rounding_ties():
+    """Values on every E2M1 tie and saturation point, with g = 1 and block
+    amax 6 so that the E4M3 scale is exactly 1 and x * (1/S) = x."""
+    spec = cases.Spec(lens=[16 + 128 * 2], seed=51, rotation=0, centering=0, key_search=0)
+    c = cases.build(spec)
+    ties = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 0.1, 0.3, 5.5, 4.5, 1.0, 0.0, 0.5, 2.0])
+    vals = ties.repeat(8)
+    sign = torch.where(torch.arange(128) % 3 == 0, -1.0, 1.0)
+    row = (vals * sign)
+    row[::16] = 6.0
+    kp = row.repeat(c.k_pages.shape[0], 128, 8, 1).to(torch.bfloat16)
+    kp[:, ::7, :, 13] = -0.0
+    c.k_pages = kp.contiguous()
+    c.v_pages = kp.flip(-1).contiguous()
+    c.gk = c.gv = 1.0
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c, pool_only=True)
+    assert np.array_equal(gpu["pool"], ora["pool"])
+
+
+def test_writer_extreme_scales():
+    """Tiny and huge per-tensor scales: E4M3 subnormal and saturated block scales."""
+    for gk, gv in ((1e-4, 3e-5), (10.0, 50.0), (1e-30, 1e30)):
+        c = cases.build(cases.Spec(lens=[16 + 128 * 3], seed=61))
+        c.gk, c.gv = gk, gv
+        gpu = cases.run_gpu(c)
+        ora = cases.run_oracle(c, pool_only=True)
+        assert np.array_equal(gpu["pool"], ora["pool"]), (gk, gv)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_writer_zero_blocks_and_extreme_magnitudes(fmt):
+    """Raw values reach the quantizer (no centering / rotation): zero blocks,
+    bf16 subnormals (MX exponent clamps at -127) and values near the bf16
+    maximum (the larger MX candidate overflows and loses the search)."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 2], seed=71, fmt=fmt, rotation=0, centering=0))
+    kp, vp = c.k_pages.clone(), c.v_pages.clone()
+    for t in (kp, vp):
+        t[0, :, :, :32] = 0.0
+        t[0, 5, 3, 32:64] = 1e-39
+        t[0, 6, 1, 64:96] = -3e-40
+        t[1, 9, 2, :] = 3e38
+        t[1, 10, 4, 96:] = -2.5e38
+    c.k_pages, c.v_pages = kp, vp
+    c.gk = c.gv = 1.0
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c, pool_only=True)
+    assert np.array_equal(gpu["pool"], ora["pool"])
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_writer_large_rotated_keys(fmt):
+    """Large keys whose Hadamard sums stay finite (128 * 1e36 < fp32 max)."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 2], seed=72, fmt=fmt))
+    kp = c.k_pages.clone()
+    kp[1, 9, 2, :] = 1e36
+    kp[1, 11, 5, ::3] = -7e35
+    c.k_pages = kp
+    c.gk = 1e34
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c, pool_only=True)
+    assert np.array_equal(gpu["pool"], ora["pool"])
+
+
+def test_bounded_wait_reports_timeout():
+    ctx = bd.Context(bd.make_config())
+    assert bd.read_device_error(ctx) == bd.OK
+    bd.selftest_bounded_wait(ctx, 20000)
+    assert bd.read_device_error(ctx) == bd.ERR_TIMEOUT
+    assert bd.read_device_error(ctx) == bd.OK     # reading resets the word
+    ctx.close()
+
+
+def test_repeat_calls_deterministic():
+    c = cases.build(cases.Spec(lens=[16 + 128 * 4 + 9], seed=81))
+    a = cases.run_gpu(c)
+    b = cases.run_gpu(c)
+    assert np.array_equal(a["pool"], b["pool"]) and np.array_equal(a["qp"], b["qp"])
+    assert np.array_equal(a["out"], b["out"])
