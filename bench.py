@@ -1,0 +1,462 @@
+"""Benchmark of the NVFP4 KV-cache hot path on one GB300 (or N replicas).
+
+Default workload (the metric's configuration): single-sequence decode at a
+131072-token context, 36 layers, 32 query / 8 KV heads, head_dim 128, full
+recipe (16-token BF16 sink, Hadamard + centered keys with {4,6} scales,
+two-term query, FP4 probabilities with c = 8, tau = 1.0), 128-token pages
+with a shuffled physical block table.  One timed step = for each of the 36
+layers, bd_quantize_query + bd_decode_attention.  The page-fill writer, which
+runs once per 128 decode steps, is timed in the same run on its own workload
+(64 sequences x 36 layers x 8 KV heads, one freshly filled 128-token page of K
+and V each) and reported as writer tokens/s.
+
+Inputs are seeded synthetic tensors (nvfp4_kv_cache_bd_gb300.synth) resident
+in HBM before timing; the 36 layers' packed pools (5.4 GB) exceed L2, so no
+explicit flush is needed.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & packed-KV HBM GB/s (% of peak) at 128K ctx; writer tok/s"
+LAYERS, HQ, HKV, D = 36, 32, 8, 128
+CTX = 131072
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--ctx", type=int, default=CTX)
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--tau", type=float, default=1.0)
+    ap.add_argument("--no-writer", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tau-sweep", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- workload ----
+
+class DecodeWorkload:
+    """Per-layer packed pools built by the library's own writer from seeded
+    bf16 K/V (generated per layer on the GPU and freed after packing)."""
+
+    def __init__(self, ctx_len, layers, tau, device, seed=0):
+        import torch
+        import nvfp4_kv_cache_bd_gb300 as bd
+        from nvfp4_kv_cache_bd_gb300 import synth
+        self.bd, self.torch = bd, torch
+        self.layers, self.tau = layers, tau
+        self.ctx = bd.Context(bd.make_config(num_layers=layers))
+        n_sink, self.npages, n_tail = synth.split_tokens(ctx_len)
+        self.seq_lens = torch.tensor([ctx_len], dtype=torch.int32, device=device)
+        self.block_table = synth.page_permutation(self.npages, seed, device).view(1, -1).contiguous()
+        self.rec = self.ctx.record_bytes
+        self.pools, self.sinks, self.tails, self.gscales, self.qs = [], [], [], [], []
+        for l in range(layers):
+            lseed = 1000 * seed + l
+            mu, mask = synth.key_mean(HKV, lseed, device)
+            k, v = synth.keys_values(ctx_len, HKV, lseed, device, mu=mu, mask=mask)
+            gk, gv = synth.gscales(k, v, mu, True, True)
+            bd.set_key_shift(self.ctx, l, mu)
+            pool = torch.empty(self.ctx.pool_bytes(self.npages), dtype=torch.uint8, device=device)
+            kp = k[16:16 + 128 * self.npages].view(self.npages, 128, HKV, D)
+            vp = v[16:16 + 128 * self.npages].view(self.npages, 128, HKV, D)
+            bd.quantize_kv_pages(self.ctx, l, kp, vp, self.block_table[0], gk, gv, pool)
+            sk = torch.zeros(1, 16, HKV, D, dtype=torch.bfloat16, device=device)
+            sv = torch.zeros_like(sk)
+            sk[0, :n_sink], sv[0, :n_sink] = k[:n_sink], v[:n_sink]
+            tk = torch.zeros(1, 128, HKV, D, dtype=torch.bfloat16, device=device)
+            tv = torch.zeros_like(tk)
+            tk[0, :n_tail], tv[0, :n_tail] = k[16 + 128 * self.npages:], v[16 + 128 * self.npages:]
+            self.pools.append(pool)
+            self.sinks.append((sk, sv))
+            self.tails.append((tk, tv))
+            self.gscales.append((gk, gv))
+            self.qs.append(synth.query(1, HQ, lseed, device))
+            del k, v, kp, vp
+        torch.cuda.synchronize()
+        self.qp = [torch.empty(1, self.ctx.query_packed_bytes, dtype=torch.uint8, device=device)
+                   for _ in range(layers)]
+        self.out = [torch.empty(1, HQ, D, dtype=torch.float32, device=device) for _ in range(layers)]
+        self.ws = torch.zeros(bd.decode_workspace_size(self.ctx, 1, self.npages) // 4 + 1, dtype=torch.float32,
+                              device=device)
+        self.bytes_per_layer = self.npages * HKV * 2 * self.rec
+
+    def layer(self, l, stream=None, q=None, ev=None):
+        bd = self.bd
+        q = self.qs[l] if q is None else q
+        bd.quantize_query(self.ctx, l, q, self.qp[l], stream)
+        if ev is not None:
+            ev[0].record()
+        sk, sv = self.sinks[l]
+        tk, tv = self.tails[l]
+        gk, gv = self.gscales[l]
+        bd.decode_attention(self.ctx, l, self.qp[l], q, self.pools[l], self.block_table, self.seq_lens, sk, sv,
+                            tk, tv, self.tau, gk, gv, self.out[l], self.ws, stream)
+        if ev is not None:
+            ev[1].record()
+
+    def step(self, stream=None, evs=None):
+        for l in range(self.layers):
+            self.layer(l, stream, ev=None if evs is None else evs[l])
+
+
+def graphed(fn, torch):
+    """Capture fn (library calls on the current stream) into a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g.replay
+
+
+def timed(fn, steps, warmup, stream, torch, dist=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        fn()
+    t1.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return t0.elapsed_time(t1) / steps
+
+
+# ------------------------------------------------------------ CPU oracle ---
+
+class OracleDecodeSample:
+    """CPU oracle's query quantization + decode on a bounded sample of one
+    layer of the workload: sample_pages FP4 pages of the 128K context plus the
+    BF16 sink and tail, built once; run() times one pass and scales it to
+    microseconds per full step (all pages, all layers)."""
+
+    def __init__(self, ctx_len, sample_pages, seed=0):
+        import numpy as np
+        import torch
+        import oracle
+        from nvfp4_kv_cache_bd_gb300 import synth
+        self.oracle, self.np = oracle, np
+        self.cfg = cfg = oracle.make_config()
+        mu, mask = synth.key_mean(HKV, seed)
+        n_sink, self.npages, n_tail = synth.split_tokens(ctx_len)
+        self.sample_pages = sample_pages
+        self.L = L = 16 + 128 * sample_pages + n_tail
+        k, v = synth.keys_values(L, HKV, seed, mu=mu, mask=mask)
+        q = synth.query(1, HQ, seed)
+        self.gk, self.gv = synth.gscales(k, v, mu, True, True)
+        u16 = lambda t: t.contiguous().view(torch.uint16).numpy()
+        self.pool = np.zeros(sample_pages * HKV * 2 * oracle.record_bytes(cfg), np.uint8)
+        self.bt = np.arange(sample_pages, dtype=np.int32).reshape(1, -1)
+        oracle.quantize_kv_pages(cfg, u16(k[16:16 + 128 * sample_pages].reshape(sample_pages, 128, HKV, D)),
+                                 u16(v[16:16 + 128 * sample_pages].reshape(sample_pages, 128, HKV, D)), self.bt[0],
+                                 mu.numpy(), self.gk, self.gv, self.pool)
+        sk = torch.zeros(1, 16, HKV, D, dtype=torch.bfloat16)
+        sk[0] = k[:16]
+        sv = torch.zeros_like(sk)
+        sv[0] = v[:16]
+        tk = torch.zeros(1, 128, HKV, D, dtype=torch.bfloat16)
+        tv = torch.zeros_like(tk)
+        tk[0, :n_tail], tv[0, :n_tail] = k[16 + 128 * sample_pages:], v[16 + 128 * sample_pages:]
+        self.args = [u16(x) for x in (q, sk, sv, tk, tv)]
+        self.mu = mu.numpy()
+
+    def describe(self):
+        return (f"oracle query + decode over {self.sample_pages} of {self.npages} FP4 pages of one layer plus the "
+                f"BF16 sink/tail, single thread, scaled x{self.npages}/{self.sample_pages} pages x {LAYERS} layers")
+
+    def run(self):
+        q, sk, sv, tk, tv = self.args
+        t = time.perf_counter()
+        qp = self.oracle.quantize_query(self.cfg, q, self.mu)
+        self.oracle.decode_attention(self.cfg, qp, q, self.mu, self.pool, self.bt, self.np.array([self.L], self.np.int32),
+                                     sk, sv, tk, tv, 1.0, self.gk, self.gv)
+        dt = time.perf_counter() - t
+        return dt * 1e6 * (self.npages / self.sample_pages) * LAYERS, dt
+
+
+# -------------------------------------------------------------- reference --
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores: each step is one
+    bounded sample of the decode workload scaled to a full step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    smp = OracleDecodeSample(args.ctx, 256)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        us, _ = smp.run()
+        if i >= args.warmup:
+            samples.append(us)
+    v = statistics.median(samples)
+    line = {"metric": METRIC, "value": v, "unit": "µs/step", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": v / 1000.0, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 attention / f32 quantizer", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"decode {args.ctx}-token ctx, batch 1, {LAYERS} layers, 32q/8kv heads, d128, "
+                                   "NVFP4 full recipe, tau 1.0", "global_batch": 1, "seq_len": args.ctx,
+                       "parallelism": "single host thread"},
+            "cpu_baseline": {"value": v, "unit": "µs/step", "cores": 1, "kind": "oracle", "sample": smp.describe()},
+            "e2e": {"value": v, "unit": "µs/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- native --
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+    import nvfp4_kv_cache_bd_gb300 as bd
+    from nvfp4_kv_cache_bd_gb300 import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    build.build_library()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    stream = torch.cuda.current_stream()
+    hbm_peak, peak_src = peaks()
+
+    # ---------------- decode workload (headline)
+    wl = DecodeWorkload(args.ctx, args.layers, args.tau, device, seed=rank)
+    fn = graphed(lambda: wl.step(), torch)   # one step = 36 x (query quantization + decode)
+    # roofline pass: events bracket each decode call (decode kernel + split combine)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = timed(fn, args.steps, args.warmup, stream, torch, pg)
+    durs = []
+    for _ in range(max(3, args.steps // 2)):
+        wl.step(evs=evs)
+        torch.cuda.synchronize()
+        durs += [a.elapsed_time(b) for a, b in evs]
+    clk = clocks.stop()
+    err = bd.read_device_error(wl.ctx)
+    if err != bd.OK:
+        raise RuntimeError(f"device error word: {bd.status_string(err)}")
+    dec_ms = statistics.mean(durs)
+    if pg is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t)
+    us_step = ms * 1000.0
+    step_bytes = wl.bytes_per_layer * args.layers
+    achieved = wl.bytes_per_layer / (dec_ms * 1e-3) / 1e9
+
+    # ---------------- end to end through the C ABI with host buffers
+    q_host = [q.cpu().pin_memory() for q in wl.qs]
+    out_host = [torch.empty(1, HQ, D, dtype=torch.float32).pin_memory() for _ in range(args.layers)]
+    q_dev = [torch.empty_like(q) for q in wl.qs]
+
+    def e2e_step():
+        for l in range(args.layers):
+            q_dev[l].copy_(q_host[l], non_blocking=True)
+            wl.layer(l, q=q_dev[l])
+            out_host[l].copy_(wl.out[l], non_blocking=True)
+
+    e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg)
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t)
+    h2d = sum(q.numel() * q.element_size() for q in q_host)
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+
+    tau_sweep = None
+    if args.tau_sweep:
+        tau_sweep = {}
+        for tau in (0.0, 0.5, 4.0, 448.0):
+            wl.tau = tau
+            tau_sweep[str(tau)] = timed(graphed(lambda: wl.step(), torch), max(5, args.steps // 2), args.warmup,
+                                        stream, torch, pg) * 1000.0
+        wl.tau = args.tau
+    del wl
+    torch.cuda.empty_cache()
+
+    # ---------------- page-fill writer workload
+    writer = None
+    if not args.no_writer:
+        writer = bench_writer(args, device, stream, torch, bd, pg, hbm_peak)
+
+    line = {
+        "metric": METRIC, "value": us_step, "unit": "µs/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 operands, f16 mma, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"decode {args.ctx}-token ctx, batch 1, {args.layers} layers, 32q/8kv heads, d128, "
+                               f"NVFP4 full recipe, tau {args.tau}, shuffled 128-token pages",
+                   "global_batch": world, "seq_len": args.ctx, "layers": args.layers,
+                   "l2": "not flushed: each step streams 36 distinct layers' pools "
+                         f"({step_bytes / 1e9:.2f} GB) >> 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "packed_kv_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "packed_kv_frac_of_peak": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (+ split combine)", "achieved": achieved,
+                     "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": None, "bytes_per_launch": wl_bytes_note(args)},
+        "e2e": {"value": e2e_ms * 1000.0, "unit": "µs/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * args.layers * 2,
+        "launch": "one CUDA graph per step (36 x query kernel + decode kernel, programmatic dependent launch)",
+        "clocks": clk,
+    }
+    if tau_sweep:
+        line["tau_sweep_us_per_step"] = tau_sweep
+    if writer:
+        line["writer"] = writer
+    if rank == 0 and not args.no_cpu_baseline:
+        smp = OracleDecodeSample(args.ctx, 256)
+        runs = [smp.run() for _ in range(3)]
+        line["cpu_baseline"] = {"value": statistics.median(r[0] for r in runs), "unit": "µs/step", "cores": 1,
+                                "kind": "oracle",
+                                "sample": smp.describe() + f"; median of 3 runs of {runs[0][1]:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def wl_bytes_note(args):
+    npages = (args.ctx - 16) // 128
+    return npages * HKV * 2 * 9216
+
+
+def bench_writer(args, device, stream, torch, bd, pg, hbm_peak):
+    from nvfp4_kv_cache_bd_gb300 import synth
+    seqs, layers = 64, args.layers
+    ctx = bd.Context(bd.make_config(num_layers=layers))
+    pools, ks, vs, gs = [], [], [], []
+    dst = synth.page_permutation(seqs, 7, device)
+    for l in range(layers):
+        mu, mask = synth.key_mean(HKV, 5000 + l, device)
+        k, v = synth.keys_values(seqs * 128, HKV, 5000 + l, device, mu=mu, mask=mask)
+        bd.set_key_shift(ctx, l, mu)
+        gs.append(synth.gscales(k, v, mu, True, True))
+        ks.append(k.view(seqs, 128, HKV, D))
+        vs.append(v.view(seqs, 128, HKV, D))
+        pools.append(torch.empty(ctx.pool_bytes(seqs), dtype=torch.uint8, device=device))
+
+    def step():
+        for l in range(layers):
+            bd.quantize_kv_pages(ctx, l, ks[l], vs[l], dst, gs[l][0], gs[l][1], pools[l])
+
+    ms = timed(graphed(step, torch), args.steps, args.warmup, stream, torch, pg)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
+    durs = []
+    for _ in range(3):
+        for l in range(layers):
+            evs[l][0].record()
+            bd.quantize_kv_pages(ctx, l, ks[l], vs[l], dst, gs[l][0], gs[l][1], pools[l])
+            evs[l][1].record()
+        torch.cuda.synchronize()
+        durs += [a.elapsed_time(b) for a, b in evs]
+    if pg is not None:
+        t = torch.tensor([ms], device=device)
+        dist_max = __import__("torch.distributed", fromlist=["all_reduce"])
+        dist_max.all_reduce(t, op=dist_max.ReduceOp.MAX)
+        ms = float(t)
+    call_bytes = seqs * 128 * HKV * D * 2 * 2 + seqs * HKV * 2 * ctx.record_bytes
+    call_ms = statistics.mean(durs)
+    tok = seqs * 128
+    return {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, NVFP4",
+            "tok_per_s": tok / (ms * 1e-3) * (pg.get_world_size() if pg is not None else 1),
+            "ms_per_step": ms, "gpu_launches_per_step": layers,
+            "roofline": {"bound": "hbm", "kernel": "writer_kernel", "achieved": call_bytes / (call_ms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": call_bytes / (call_ms * 1e-3) / 1e9 / hbm_peak,
+                         "bytes_per_launch": call_bytes}}
+
+
+if __name__ == "__main__":
+    main()

@@ -185,7 +185,10 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *   k/v_gscale  : the per-tensor scales the layer's pages were written with.
  *   out         : fp32 [B][num_q_heads][128], device.
  *   ws          : device scratch of at least bd_decode_workspace_size(ctx, B,
- *                 max_blocks) bytes; its contents need no initialisation.
+ *                 max_blocks) bytes.  Its first bytes hold split tickets:
+ *                 zero the whole workspace once before its first use; every
+ *                 completed call leaves the tickets zero again.  Calls that
+ *                 share a workspace must not overlap on the GPU.
  * Query head j reads kv head j / 4; softmax scale 1/sqrt(128). */
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q,
                         const void* kv_pool, const int32_t* block_table, int max_blocks,

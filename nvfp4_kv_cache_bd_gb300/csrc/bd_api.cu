@@ -163,7 +163,7 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks) {
     if (!ctx || B <= 0 || max_blocks < 0) return 0;
     int ns = 0, pps = 0;
     bd::decode_splits(B, ctx->cfg.num_kv_heads, max_blocks, &ns, &pps);
-    return (size_t)B * ctx->cfg.num_q_heads * (ns + 1) * bd::kPartStride * sizeof(float);
+    return bd::decode_ws_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ns);
 }
 
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q, const void* kv_pool,
@@ -196,7 +196,8 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     a.tail_k = static_cast<const uint16_t*>(tail_k);
     a.tail_v = static_cast<const uint16_t*>(tail_v);
     a.out = out;
-    a.ws = static_cast<float*>(ws);
+    a.counters = static_cast<int*>(ws);
+    a.parts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + bd::decode_counter_bytes(B, ctx->cfg.num_kv_heads));
     a.err = ctx->d_err;
     a.qstride = bd::qpack_stride(ctx->cfg.num_q_heads);
     a.B = B;

@@ -1,6 +1,6 @@
 // Paged single-token decode attention over the hybrid cache (BF16 sink +
-// packed FP4 pages + BF16 tail), flash-decoding style split-K over pages,
-// and the split combine.
+// packed FP4 pages + BF16 tail): flash-decoding split-K over pages with the
+// split combine done by the last CTA of each (sequence, kv head).
 //
 // Method: "How openbitsys/bitdecoding-fp4 works" (decode interface -> paged
 // attention kernel; hybrid cache); BitDecoding-FP4 evaluation config
@@ -8,14 +8,17 @@
 // probability_environment ("amax6" / "amax2_or_amax6" with c in {1, 8} and
 // tau in [0, 448]), RECIPE dual_residual_query_quantization (two query terms).
 //
-// Grid (nsplit + 1, kv heads, sequences).  Split 0 of a (sequence, kv head)
-// handles the BF16 sink and tail tokens with exact probabilities; splits
-// 1..nsplit each stream a contiguous range of that sequence's FP4 pages.
+// Grid (nsplit + 1, kv heads, sequences), 160 threads.  Split 0 of a
+// (sequence, kv head) handles the BF16 sink and tail tokens with exact
+// probabilities; splits 1..nsplit each stream a contiguous range of that
+// sequence's FP4 pages.
 //
 // FP4 split CTA: warp 4 is the producer; one elected lane streams each
-// page's K and V records (9216 B each in NVFP4) into a 4-stage shared-memory
-// ring with cp.async.bulk, completing on per-stage "full" mbarriers; warps
-// 0..3 consume.  Consumer warp w owns tokens 32w..32w+31 of every page:
+// page's K and V records (9216 B each in NVFP4) into a 6-stage shared-memory
+// ring with cp.async.bulk (TMA), completing on per-stage "full" mbarriers.
+// Warps 0..3 consume whole pages round-robin (page k -> warp k % 4), so a
+// page's softmax maximum never crosses warps and each warp carries eight
+// independent 16-token blocks through every phase:
 //  QK  : m16n8k16 f16 MMAs, M = 16 tokens, N = 8 = 4 query heads x 2 query
 //        terms, K = 16 head dims.  FP4 codes are widened by cvt e2m1x2->f16x2
 //        and multiplied by their E4M3 scale in f16, which is exact
@@ -23,18 +26,21 @@
 //        [2^-10, 2688]); the query terms are exact the same way.  Per-tensor
 //        scales, the 1/sqrt(128) softmax scale and q.mu are applied to the
 //        fp32 accumulators.
-//  P   : per page, the page maximum m_p of every head (the four warps trade
-//        their maxima through shared memory at one named barrier); P =
-//        exp(s - m_p); each 16-token block is quantized to FP4 with the
-//        amax2-or-amax6 rule; Phat = E2M1 x E4M3 / c is again exact in f16.
-//  PV  : O^T[128 dims][8] += Vhat^T[dims][16 tokens] Phat^T, V codes widened
-//        and scaled exactly as for K.  The V record stores tokens tau and
-//        tau+8 in one byte, which is exactly an A-fragment register of this
-//        MMA; Phat reaches the B-fragment layout with two warp shuffles.
-//  The page partial (m_p, l_p, O_p) is merged into a running (M, L, O) per
-//  warp; at the end the four warps' partials are summed through shared
-//  memory and written to the workspace.
-// The combine kernel merges all splits: O = sum e^(m-M) O / sum e^(m-M) l.
+//  P   : the page maximum m_p of every head (warp shuffles); P = exp(s - m_p);
+//        each 16-token block is quantized to FP4 with the amax2-or-amax6 rule;
+//        Phat = E2M1 x E4M3 / c is again exact in f16.
+//  PV  : O^T[128 dims][8] += Vhat^T[dims][16 tokens] Phat^T.  The V record
+//        stores tokens tau and tau+8 in one byte, which is exactly an
+//        A-fragment register of this MMA; Phat reaches the B-fragment layout
+//        with two warp shuffles.
+//  Each warp merges its pages into a running (M, L, O); at the end the four
+//  warps' states are merged through shared memory into the split partial.
+// The last CTA to finish a (sequence, kv head) -- an atomic ticket in the
+// workspace -- merges all splits: O = sum 2^(m-M) O / sum 2^(m-M) l.
+//
+// Launched with programmatic dependent launch: the producer starts streaming
+// pages while the query quantizer still runs; every thread that reads the
+// packed or raw query first waits on the preceding grid.
 #include <math.h>
 
 #include "bd_device.cuh"
@@ -43,29 +49,41 @@ namespace bd {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMaxRec = 9216;
 constexpr int kStageBytes = 2 * kMaxRec;
 constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kMaxSplits = 1024;
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 struct Ctl {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
-    float red[2][kConsumers][4];
-    int vote[2][kConsumers];   // per page: 1 if that warp's wait for the page gave up
-    int abort_flag;            // hint that lets pending waits give up early
+    float wm[kConsumers][4];   // per-warp running max per head (log2 units)
+    float wl[kConsumers][4];   // per-warp softmax denominator per head
+    int abort_flag;
     int issued;
-    int consumed[kConsumers];
+    int consumed[kConsumers];  // first page index each warp did not consume
+    int is_last;
 };
-constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl);
+constexpr int kScratchBytes = kConsumers * 8 * 2 * 32 * 4;   // per-warp score scratch
+constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes;
+static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
+static_assert(sizeof(Ctl) % 16 == 0, "score scratch must stay 16-byte aligned");
 
 __device__ __forceinline__ float ex2(float x) {
     float r;
     asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -84,14 +102,12 @@ __device__ __forceinline__ uint32_t f16_pow2(int k) {
     return 0u;
 }
 
-__device__ __forceinline__ void write_empty(float* part, int nsplit1) {
-    for (int hh = 0; hh < 4; ++hh) {
-        part[hh * nsplit1 * kPartStride + 0] = -INFINITY;
-        part[hh * nsplit1 * kPartStride + 1] = 0.0f;
-    }
-}
-
 // ------------------------------------------------------ BF16 sink + tail --
+
+// Shared-memory row pitch of a staged bf16 head vector: 256 B plus 16 B so
+// that eight consecutive rows read with 16-byte loads hit distinct banks.
+constexpr int kRowPitch = 272;
+constexpr int kMaxBf16Tok = kSink + kPage - 1;   // 143
 
 __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* part, uint8_t* smem) {
     const int ns = min(L, kSink);
@@ -102,31 +118,49 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
     const int nsplit1 = a.nsplit + 1;
     const int tid = threadIdx.x;
     if (T == 0) {
-        if (tid == 0) write_empty(part, nsplit1);
+        if (tid < 4) {
+            part[tid * nsplit1 * kPartStride + 0] = -INFINITY;
+            part[tid * nsplit1 * kPartStride + 1] = 0.0f;
+        }
         return;
     }
-    float* qf = reinterpret_cast<float*>(smem);      // [4][128]
-    float* sp = qf + 4 * kD;                          // [4][144]
-    float* mh = sp + 4 * 144;                         // [4]
-    float* lh = mh + 4;                               // [4]
-    for (int i = tid; i < 4 * kD; i += blockDim.x) {
-        const uint16_t bits = a.q[((size_t)b * a.hq + 4 * h + i / kD) * kD + (i % kD)];
-        qf[i] = __uint_as_float((uint32_t)bits << 16);
+    uint8_t* ks = smem;                                            // [T][272 B] bf16 keys
+    uint8_t* vs = ks + kMaxBf16Tok * kRowPitch;                    // [T][272 B] bf16 values
+    float* qf = reinterpret_cast<float*>(vs + kMaxBf16Tok * kRowPitch);   // [4][128]
+    float* sp = qf + 4 * kD;                                       // [4][144] scores, then P
+    float* mh = sp + 4 * 144;                                      // [4]
+    float* lh = mh + 4;                                            // [4]
+    // stage the sink and tail rows of this kv head with asynchronous 16-byte
+    // copies (no thread waits for one load before issuing the next)
+    for (int i = tid; i < T * 16; i += blockDim.x) {
+        const int tau = i >> 4, c = i & 15;
+        const size_t krow = tau < ns ? (((size_t)b * kSink + tau) * a.hkv + h) * kD
+                                     : (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
+        const uint16_t* kb = (tau < ns ? a.sink_k : a.tail_k) + krow + 8 * c;
+        const uint16_t* vb = (tau < ns ? a.sink_v : a.tail_v) + krow + 8 * c;
+        cp_async16(smem_u32(ks + tau * kRowPitch + 16 * c), kb);
+        cp_async16(smem_u32(vs + tau * kRowPitch + 16 * c), vb);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    griddep_wait();
+    if (tid < 4 * kD / 8) {
+        const int hh = tid >> 4, c = tid & 15;
+        const uint4 u = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.hq + 4 * h + hh) * kD + 8 * c);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            qf[hh * kD + 8 * c + 2 * e] = bf16_lo(wd[e]);
+            qf[hh * kD + 8 * c + 2 * e + 1] = bf16_hi(wd[e]);
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    auto krow = [&](int tau) -> const uint16_t* {
-        return tau < ns ? a.sink_k + (((size_t)b * kSink + tau) * a.hkv + h) * kD
-                        : a.tail_k + (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
-    };
-    auto vrow = [&](int tau) -> const uint16_t* {
-        return tau < ns ? a.sink_v + (((size_t)b * kSink + tau) * a.hkv + h) * kD
-                        : a.tail_v + (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
-    };
+    // scores: one thread per token, four heads
     for (int tau = tid; tau < T; tau += blockDim.x) {
-        const uint4* kr = reinterpret_cast<const uint4*>(krow(tau));
         float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
         for (int c = 0; c < 16; ++c) {
-            const uint4 u = kr[c];
+            const uint4 u = *reinterpret_cast<const uint4*>(ks + tau * kRowPitch + 16 * c);
             const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -160,10 +194,12 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
         }
     }
     __syncthreads();
+    // O = P V: one thread per head dim, four heads
     if (tid < kD) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
         for (int tau = 0; tau < T; ++tau) {
-            const float v = __uint_as_float((uint32_t)vrow(tau)[tid] << 16);
+            const float v = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(vs + tau * kRowPitch + 2 * tid)) << 16);
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) acc[hh] = fmaf(sp[hh * 144 + tau], v, acc[hh]);
         }
@@ -179,152 +215,95 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
     }
 }
 
-// --------------------------------------------------------- FP4 page split --
+// ------------------------------------------------ FP4 page split: consumer --
 
-template <int FMT>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int L = a.seq_lens[b];
-    const int nsplit1 = a.nsplit + 1;
-    float* part = a.ws + ((size_t)(b * a.hq + 4 * h) * nsplit1 + split) * kPartStride;
-
-    if (split == 0) {
-        bf16_segment(a, b, h, L, part, smem);
-        return;
-    }
-    // pages past the block-table row are ignored (the header bounds L)
-    const int npages = min(max(0, L - kSink) / kPage, a.max_blocks);
-    const int p0 = (split - 1) * a.pages_per_split;
-    const int p1 = min(p0 + a.pages_per_split, npages);
-    if (p0 >= p1) {
-        if (threadIdx.x == 0) write_empty(part, nsplit1);
-        return;
-    }
-    const int n = p1 - p0;
-    constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), kConsumers);
+template <int FMT, int PM>
+__device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t* smem, Ctl* ctl, int warp,
+                              int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    // this warp's score scratch: [8 blocks][2 tokens][32 lanes] fp32
+    float* sS = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl)) + warp * (8 * 2 * 32);
+    griddep_wait();
+    const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
+    const int hq = a.hq;
+    // B fragments of the query: row n = g -> head 4h + g/2, term g%2; this
+    // lane's k-slots are head dims 32t .. 32t+31.
+    uint32_t qB[16];
+    float qx[2];   // MXFP4: 2^(reference exponent) of this lane's two C columns
+    {
+        const int jq = 4 * h + (g >> 1), term = g & 1;
+        const uint4 qc = *reinterpret_cast<const uint4*>(qrec + (term * hq + jq) * 64 + 16 * t);
+        uint32_t slo, shi;
+        if (FMT == BD_FORMAT_NVFP4) {
+            const uint32_t qsd = e4m3x2_to_f16x2(
+                *reinterpret_cast<const uint16_t*>(qrec + 2 * hq * 64 + (term * hq + jq) * 8 + 2 * t));
+            slo = bcast_lo(qsd);
+            shi = bcast_hi(qsd);
+        } else {
+            const uint32_t e4 = *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term * hq + jq) * 4);
+            int emax = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) emax = max(emax, (int)((e4 >> (8 * q)) & 0xFF));
+            slo = shi = bcast_lo(f16_pow2((int)((e4 >> (8 * t)) & 0xFF) - emax));
         }
-        ctl->abort_flag = 0;
-        ctl->issued = 0;
-        fence_mbar_init();
-    }
-    if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
-    __syncthreads();
-
-    if (warp == kConsumers) {
-        // ------------------------------------------------------ producer --
-        if (lane == 0) {
-            const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
-            const size_t rec_stride = (size_t)RB;
-            int k = 0;
-            for (; k < n; ++k) {
-                const int s = k % kStages;
-                if (k >= kStages) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ((k / kStages) - 1) & 1, kWaitLimitNs,
-                                           &ctl->abort_flag)) {
-                        if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
-                        ctl->abort_flag = 1;
-                        break;
-                    }
-                }
-                const int64_t phys = bt[k];
-                const uint8_t* krec = a.pool + ((phys * a.hkv + h) * 2) * rec_stride;
-                const uint32_t full = smem_u32(&ctl->full[s]);
-                const uint32_t dst = smem_u32(smem + s * kStageBytes);
-                mbar_arrive_expect_tx(full, 2 * RB);
-                bulk_g2s(dst, krec, RB, full);
-                bulk_g2s(dst + kMaxRec, krec + RB, RB, full);
-            }
-            ctl->issued = k;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t pr = byte_pair(qc, kk);
+            const uint32_t sc = kk < 4 ? slo : shi;
+            qB[2 * kk] = hmul2(e2m1x2_to_f16x2(pr & 0xFF), sc);
+            qB[2 * kk + 1] = hmul2(e2m1x2_to_f16x2(pr >> 8), sc);
         }
-    } else {
-        // ------------------------------------------------------ consumers --
-        const int g = lane >> 2, t = lane & 3;
-        const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
-        const int hq = a.hq;
-        // B fragments of the query: row n = g -> head 4h + g/2, term g%2;
-        // this lane's k-slots are head dims 32t .. 32t+31.
-        uint32_t qB[16];
-        float qx[2];   // MXFP4: 2^(row reference exponent) of this lane's C columns
-        {
-            const int jq = 4 * h + (g >> 1), term = g & 1;
-            const uint4 qc = *reinterpret_cast<const uint4*>(qrec + (term * hq + jq) * 64 + 16 * t);
-            uint32_t slo, shi;
-            if (FMT == BD_FORMAT_NVFP4) {
-                const uint32_t qsd = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(
-                    qrec + 2 * hq * 64 + (term * hq + jq) * 8 + 2 * t));
-                slo = bcast_lo(qsd);
-                shi = bcast_hi(qsd);
-            } else {
-                const uint32_t e4 = *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term * hq + jq) * 4);
+        qx[0] = qx[1] = 1.0f;
+        if (FMT == BD_FORMAT_MXFP4) {
+#pragma unroll
+            for (int term2 = 0; term2 < 2; ++term2) {
+                const uint32_t e4 =
+                    *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term2 * hq + 4 * h + t) * 4);
                 int emax = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) emax = max(emax, (int)((e4 >> (8 * q)) & 0xFF));
-                const int et = (int)((e4 >> (8 * t)) & 0xFF);
-                slo = shi = bcast_lo(f16_pow2(et - emax));
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t pr = byte_pair(qc, kk);
-                const uint32_t sc = kk < 4 ? slo : shi;
-                qB[2 * kk] = hmul2(e2m1x2_to_f16x2(pr & 0xFF), sc);
-                qB[2 * kk + 1] = hmul2(e2m1x2_to_f16x2(pr >> 8), sc);
-            }
-            if (FMT == BD_FORMAT_MXFP4) {
-#pragma unroll
-                for (int term2 = 0; term2 < 2; ++term2) {
-                    const uint32_t e4 =
-                        *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term2 * hq + 4 * h + t) * 4);
-                    int emax = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) emax = max(emax, (int)((e4 >> (8 * q)) & 0xFF));
-                    qx[term2] = pow2i(emax - 127);
-                }
-            } else {
-                qx[0] = qx[1] = 1.0f;
+                qx[term2] = pow2i(emax - 127);
             }
         }
-        const float* gq = reinterpret_cast<const float*>(qrec + 2 * hq * 64 + 2 * hq * 8);
-        const float gK = (FMT == BD_FORMAT_NVFP4) ? a.gk : 1.0f;
-        const float gV = (FMT == BD_FORMAT_NVFP4) ? a.gv : 1.0f;
-        const float a1 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[0] : qx[0]);
-        const float a2 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[1] : qx[1]);
-        const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + t] : 0.0f;
-        const int cc = (a.p_mode == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1;
-        const float ccf = (float)cc;
-        const uint32_t inv_cc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / ccf)));
+    }
+    const float* gq = reinterpret_cast<const float*>(qrec + 2 * hq * 64 + 2 * hq * 8);
+    const float gK = (FMT == BD_FORMAT_NVFP4) ? a.gk : 1.0f;
+    const float gV = (FMT == BD_FORMAT_NVFP4) ? a.gv : 1.0f;
+    const float a1 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[0] : qx[0]);
+    const float a2 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[1] : qx[1]);
+    const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + t] : 0.0f;
+    const float ccf = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
+    const float tau = a.tau;
+    const uint32_t inv_cc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / ccf)));
+    const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
+    const int gs = g & 3;
 
-        float M[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float o[8][4];
+    float Mt = -INFINITY, MA = -INFINITY, MB = -INFINITY;   // running max of heads t, 2t, 2t+1
+    float lacc = 0.0f;
+    float o[8][4];
 #pragma unroll
-        for (int bm = 0; bm < 8; ++bm) o[bm][0] = o[bm][1] = o[bm][2] = o[bm][3] = 0.0f;
-        float lacc = 0.0f;
+    for (int bm = 0; bm < 8; ++bm) o[bm][0] = o[bm][1] = o[bm][2] = o[bm][3] = 0.0f;
 
-        int k = 0;
-        for (; k < n; ++k) {
-            const int s = k % kStages;
-            const bool ok =
-                mbar_wait_bounded(smem_u32(&ctl->full[s]), (k / kStages) & 1, kWaitLimitNs, &ctl->abort_flag);
-            if (!ok) {
-                if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
-                ctl->abort_flag = 1;
-            }
-            const uint8_t* Ks = smem + s * kStageBytes;
-            const uint8_t* Vs = Ks + kMaxRec;
+    int k = warp;
+    for (; k < n; k += kConsumers) {
+        const int s = k % kStages;
+        if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), (k / kStages) & 1, kWaitLimitNs, &ctl->abort_flag)) {
+            if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+            ctl->abort_flag = 1;
+            break;
+        }
+        const uint8_t* Ks = smem + s * kStageBytes;
+        const uint8_t* Vs = Ks + kMaxRec;
 
-            // ---------------- QK: scores (log2 units) for head t, tokens
-            // 32w + 16 mi + g (+8)
-            float sc[2][2];
+        // ---------------- QK, two 16-token blocks per iteration: log2-scaled
+        // scores of head t for tokens 16mi+g and 16mi+g+8 go to the scratch
+        float mp = -INFINITY;
+#pragma unroll 1
+        for (int m2 = 0; m2 < 8; m2 += 2) {
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-                const int tok0 = 16 * (2 * warp + mi) + g, tok1 = tok0 + 8;
+            for (int u = 0; u < 2; ++u) {
+                const int mi = m2 + u;
+                const int tok0 = 16 * mi + g, tok1 = tok0 + 8;
                 const uint4 c0 = lds128(Ks + tok0 * 64 + 16 * t);
                 const uint4 c1 = lds128(Ks + tok1 * 64 + 16 * t);
                 uint32_t s0lo, s0hi, s1lo, s1hi;
@@ -359,87 +338,71 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                     A[3] = hmul2(e2m1x2_to_f16x2(p1w >> 8), sb2);
                     mma16816(acc, A, qB[2 * kk], qB[2 * kk + 1]);
                 }
-                sc[mi][0] = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
-                sc[mi][1] = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
+                const float s0 = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
+                const float s1 = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
+                sS[(2 * mi) * 32 + lane] = s0;
+                sS[(2 * mi + 1) * 32 + lane] = s1;
+                mp = fmaxf(mp, fmaxf(s0, s1));
             }
+        }
 
-            // ---------------- page maximum per head (all four warps)
-            float mloc = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-            mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 4));
-            mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 8));
-            mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, 16));
-            if (g == 0) ctl->red[k & 1][warp][t] = mloc;
-            if (lane == 0) ctl->vote[k & 1][warp] = ok ? 0 : 1;
-            named_bar_sync(1, kConsumers * 32);
-            // every consumer warp reads the same four votes: the break is uniform
-            if (ctl->vote[k & 1][0] | ctl->vote[k & 1][1] | ctl->vote[k & 1][2] | ctl->vote[k & 1][3]) break;
-            float mp[4];
-            {
-                const float4 r0 = *reinterpret_cast<const float4*>(ctl->red[k & 1][0]);
-                const float4 r1 = *reinterpret_cast<const float4*>(ctl->red[k & 1][1]);
-                const float4 r2 = *reinterpret_cast<const float4*>(ctl->red[k & 1][2]);
-                const float4 r3 = *reinterpret_cast<const float4*>(ctl->red[k & 1][3]);
-                mp[0] = fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x));
-                mp[1] = fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y));
-                mp[2] = fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z));
-                mp[3] = fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w));
-            }
-            const float mpt = (t == 0) ? mp[0] : (t == 1) ? mp[1] : (t == 2) ? mp[2] : mp[3];
+        // ---------------- page maximum of head t (and of heads 2t, 2t+1)
+        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 4));
+        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 8));
+        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 16));
+        const float mpA = __shfl_sync(kFull, mp, srcA), mpB = __shfl_sync(kFull, mp, srcB);
 
-            // ---------------- probabilities and their FP4 quantization
-            uint32_t pv[2];
-            float lpage = 0.0f;
+        float fv = 1.0f;   // MXFP4: 2^(reference exponent of this lane's V block)
+        int ev_ref = 0;
+        if (FMT == BD_FORMAT_MXFP4) {
+            int em = 0;
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-                const float p0 = ex2(sc[mi][0] - mpt), p1 = ex2(sc[mi][1] - mpt);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
+                const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
+                em = max(em, (int)max(max(e0 & 0xFF, e0 >> 8), max(e1 & 0xFF, e1 >> 8)));
+            }
+            em = max(em, __shfl_xor_sync(kFull, em, 1));
+            em = max(em, __shfl_xor_sync(kFull, em, 2));
+            em = max(em, __shfl_xor_sync(kFull, em, 4));
+            ev_ref = em;
+            fv = pow2i(em - 127);
+        }
+
+        // ---------------- per 16-token block: probabilities, their FP4
+        // quantization, and P V into O_p^T[dims][heads]
+        float op[8][4];
+#pragma unroll
+        for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
+        float lpage = 0.0f;
+#pragma unroll 1
+        for (int i2 = 0; i2 < 8; i2 += 2) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i2 + u;
+                const float p0 = ex2(sS[(2 * i) * 32 + lane] - mp), p1 = ex2(sS[(2 * i + 1) * 32 + lane] - mp);
                 lpage += p0 + p1;
-                if (a.p_mode == BD_P_NONE) {
+                uint32_t pv;
+                if (PM == BD_P_NONE) {
                     const __half2 hh = __floats2half2_rn(p0, p1);
-                    pv[mi] = *reinterpret_cast<const uint32_t*>(&hh);
+                    pv = *reinterpret_cast<const uint32_t*>(&hh);
                 } else {
                     const float u0 = p0 * ccf, u1 = p1 * ccf;
                     float am = fmaxf(u0, u1);
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 4));
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 8));
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 16));
-                    const float mode = (a.p_mode == BD_P_AMAX2_OR_AMAX6 && am < a.tau) ? 2.0f : 6.0f;
-                    const uint32_t sbyte = e4m3(__fdiv_rn(am, mode));
-                    const uint32_t sdh = e4m3x2_to_f16x2(sbyte);
+                    const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (am < tau);
+                    const float sv = two ? am * 0.5f : __fdiv_rn(am, 6.0f);
+                    const uint32_t sdh = e4m3x2_to_f16x2(e4m3(sv));
                     const float sd = __half2float(__ushort_as_half((unsigned short)(sdh & 0xFFFF)));
                     const float inv = __frcp_rn(sd);
                     const bool zero = (sd == 0.0f) || isinf(inv);
                     const uint32_t byte = zero ? 0u : e2m1x2(__fmul_rn(u0, inv), __fmul_rn(u1, inv));
-                    pv[mi] = hmul2(e2m1x2_to_f16x2(byte), hmul2(bcast_lo(sdh), inv_cc));
+                    pv = hmul2(e2m1x2_to_f16x2(byte), hmul2(bcast_lo(sdh), inv_cc));
                 }
-            }
-
-            // ---------------- PV: O_p^T[dims][heads] for this warp's 32 tokens
-            float op[8][4];
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
-            float fv = 1.0f;    // MXFP4: 2^(reference exponent of this lane's V block)
-            int ev_ref = 0;
-            if (FMT == BD_FORMAT_MXFP4) {
-                int em = 0;
-#pragma unroll
-                for (int mi = 0; mi < 2; ++mi) {
-                    const int i = 2 * warp + mi;
-                    const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
-                    const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
-                    em = max(em, (int)max(max(e0 & 0xFF, e0 >> 8), max(e1 & 0xFF, e1 >> 8)));
-                }
-                em = max(em, __shfl_xor_sync(kFull, em, 1));
-                em = max(em, __shfl_xor_sync(kFull, em, 2));
-                em = max(em, __shfl_xor_sync(kFull, em, 4));
-                ev_ref = em;
-                fv = pow2i(em - 127);
-            }
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-                const int i = 2 * warp + mi;
-                const int gs = g & 3;
-                uint32_t b01 = __shfl_sync(kFull, pv[mi], 4 * t + gs);
-                uint32_t b23 = __shfl_sync(kFull, pv[mi], 16 + 4 * t + gs);
+                uint32_t b01 = __shfl_sync(kFull, pv, 4 * t + gs);
+                uint32_t b23 = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
                 if (g >= 4) b01 = b23 = 0u;
                 const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * g);
                 const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * g);
@@ -464,108 +427,224 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                     mma16816(op[bm], A, b01, b23);
                 }
             }
-            // release the stage: every lane's shared-memory reads are done
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
-
-            // ---------------- merge the page into the running state
-            float al[4], be[4];
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                const float mn = fmaxf(M[hh], mp[hh]);
-                al[hh] = ex2(M[hh] - mn);
-                be[hh] = ex2(mp[hh] - mn);
-                M[hh] = mn;
-            }
-            // this lane's O columns are heads 2t, 2t+1 (t >= 2: padding columns)
-            const bool odd = (t & 1) != 0;
-            const float aA = odd ? al[2] : al[0], aB = odd ? al[3] : al[1];
-            const float bA = (odd ? be[2] : be[0]) * gV * fv, bB = (odd ? be[3] : be[1]) * gV * fv;
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) {
-                o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
-                o[bm][1] = fmaf(o[bm][1], aB, bB * op[bm][1]);
-                o[bm][2] = fmaf(o[bm][2], aA, bA * op[bm][2]);
-                o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
-            }
-            const float at = (t == 0) ? al[0] : (t == 1) ? al[1] : (t == 2) ? al[2] : al[3];
-            const float bt2 = (t == 0) ? be[0] : (t == 1) ? be[1] : (t == 2) ? be[2] : be[3];
-            lacc = fmaf(lacc, at, bt2 * lpage);
         }
-        if (lane == 0) ctl->consumed[warp] = k;
+        // release the stage: every lane's shared-memory reads are done
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
 
-        // ---------------- per-warp partials to shared memory
-        __syncthreads();   // (A) every consumer is done with the ring
-        float* sO = reinterpret_cast<float*>(smem);          // [4 warps][4 heads][128]
-        float* sL = sO + kConsumers * 4 * kD;                // [4 warps][4 heads]
-        if (t < 2) {
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) {
-                const int d = 16 * g + 2 * bm;
-                sO[(warp * 4 + 2 * t) * kD + d] = o[bm][0];
-                sO[(warp * 4 + 2 * t + 1) * kD + d] = o[bm][1];
-                sO[(warp * 4 + 2 * t) * kD + d + 1] = o[bm][2];
-                sO[(warp * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3];
-            }
-        }
-        lacc += __shfl_xor_sync(kFull, lacc, 4);
-        lacc += __shfl_xor_sync(kFull, lacc, 8);
-        lacc += __shfl_xor_sync(kFull, lacc, 16);
-        if (g == 0) sL[warp * 4 + t] = lacc;
-        named_bar_sync(1, kConsumers * 32);
+        // ---------------- merge the page into the warp's running state
         {
-            const int hh = threadIdx.x >> 5, d0 = (threadIdx.x & 31) * 4;
-            float* ph = part + hh * nsplit1 * kPartStride;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kConsumers; ++w) {
-                const float4 v = *reinterpret_cast<const float4*>(&sO[(w * 4 + hh) * kD + d0]);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            const bool aborted = ctl->abort_flag != 0;
-            *reinterpret_cast<float4*>(&ph[4 + d0]) = acc;
-            if ((threadIdx.x & 31) == 0) {
-                const float mh = (hh == 0) ? M[0] : (hh == 1) ? M[1] : (hh == 2) ? M[2] : M[3];
-                ph[0] = aborted ? -INFINITY : mh;
-                ph[1] = aborted ? 0.0f : (sL[hh] + sL[4 + hh] + sL[8 + hh] + sL[12 + hh]);
-            }
+            const float mn = fmaxf(Mt, mp);
+            lacc = fmaf(lacc, ex2(Mt - mn), ex2(mp - mn) * lpage);
+            Mt = mn;
         }
-        return;
+        const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
+        const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
+        const float bA = ex2(mpA - mnA) * gV * fv, bB = ex2(mpB - mnB) * gV * fv;
+        MA = mnA;
+        MB = mnB;
+#pragma unroll
+        for (int bm = 0; bm < 8; ++bm) {
+            o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
+            o[bm][1] = fmaf(o[bm][1], aB, bB * op[bm][1]);
+            o[bm][2] = fmaf(o[bm][2], aA, bA * op[bm][2]);
+            o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
+        }
+        __syncwarp();   // the scratch is rewritten by the next page
     }
-    // producer warp: meet the consumers at (A), then drain copies that an
-    // aborted run left in flight before the CTA's shared memory is released.
-    __syncthreads();
-    if (lane == 0 && ctl->abort_flag) {
-        int done = n;
-        for (int w = 0; w < kConsumers; ++w) done = min(done, ctl->consumed[w]);
-        for (int kk = done; kk < ctl->issued; ++kk)
-            (void)mbar_wait_bounded(smem_u32(&ctl->full[kk % kStages]), (kk / kStages) & 1, kWaitLimitNs, nullptr);
+    if (lane == 0) ctl->consumed[warp] = k;
+
+    // ---------------- hand the warp state to the CTA merge
+    __syncthreads();   // (A) all consumers are done with the ring
+    float* sO = reinterpret_cast<float*>(smem);   // [4 warps][4 heads][128]
+    if (t < 2) {
+#pragma unroll
+        for (int bm = 0; bm < 8; ++bm) {
+            const int d = 16 * g + 2 * bm;
+            sO[(warp * 4 + 2 * t) * kD + d] = o[bm][0];
+            sO[(warp * 4 + 2 * t + 1) * kD + d] = o[bm][1];
+            sO[(warp * 4 + 2 * t) * kD + d + 1] = o[bm][2];
+            sO[(warp * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3];
+        }
+    }
+    lacc += __shfl_xor_sync(kFull, lacc, 4);
+    lacc += __shfl_xor_sync(kFull, lacc, 8);
+    lacc += __shfl_xor_sync(kFull, lacc, 16);
+    if (g == 0) {
+        ctl->wm[warp][t] = Mt;
+        ctl->wl[warp][t] = lacc;
     }
 }
 
-// ----------------------------------------------------------------- combine --
-
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
-    const int j = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+// CTA merge of the four warps' states into this split's partial.
+__device__ void write_split_partial(const DecodeArgs& a, float* part, const uint8_t* smem, const Ctl* ctl) {
+    const int tid = threadIdx.x;
+    if (tid >= 128) return;
+    const int hh = tid >> 5, d0 = (tid & 31) * 4;
     const int nsplit1 = a.nsplit + 1;
-    const float* parts = a.ws + (size_t)(b * a.hq + j) * nsplit1 * kPartStride;
+    const float* sO = reinterpret_cast<const float*>(smem);
     float M = -INFINITY;
-    for (int s = 0; s < nsplit1; ++s)
-        if (parts[s * kPartStride + 1] > 0.0f) M = fmaxf(M, parts[s * kPartStride]);
-    float num = 0.0f, den = 0.0f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < nsplit1; ++s) {
-            const float* p = parts + s * kPartStride;
-            if (!(p[1] > 0.0f)) continue;
-            const float w = ex2(p[0] - M);
-            den = fmaf(w, p[1], den);
-            num = fmaf(w, p[4 + d], num);
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ctl->wm[w][hh]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+        const float e = (ctl->wm[w][hh] == -INFINITY) ? 0.0f : ex2(ctl->wm[w][hh] - M);
+        const float4 v = *reinterpret_cast<const float4*>(&sO[(w * 4 + hh) * kD + d0]);
+        acc.x = fmaf(e, v.x, acc.x);
+        acc.y = fmaf(e, v.y, acc.y);
+        acc.z = fmaf(e, v.z, acc.z);
+        acc.w = fmaf(e, v.w, acc.w);
+        L = fmaf(e, ctl->wl[w][hh], L);
+    }
+    float* ph = part + hh * nsplit1 * kPartStride;
+    *reinterpret_cast<float4*>(&ph[4 + d0]) = acc;
+    if ((tid & 31) == 0) {
+        const bool aborted = ctl->abort_flag != 0 || M == -INFINITY;
+        ph[0] = aborted ? -INFINITY : M;
+        ph[1] = aborted ? 0.0f : L;
+    }
+}
+
+// Merge every split of (b, kv head h) into out (run by the last CTA).
+__device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem) {
+    const int nsplit1 = a.nsplit + 1;
+    float* sm = reinterpret_cast<float*>(smem);            // [4][nsplit1] m
+    float* sl = sm + 4 * nsplit1;                          // [4][nsplit1] l
+    const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
+    for (int i = threadIdx.x; i < 4 * nsplit1; i += blockDim.x) {
+        const float* p = base + (size_t)i * kPartStride;   // i = hh * nsplit1 + s
+        const float l = __ldcg(p + 1);
+        sl[i] = l;
+        sm[i] = (l > 0.0f) ? __ldcg(p) : -INFINITY;
+    }
+    __syncthreads();
+    const int tid = threadIdx.x;
+    if (tid < kD) {
+#pragma unroll 1
+        for (int hh = 0; hh < 4; ++hh) {
+            float M = -INFINITY;
+            for (int s = 0; s < nsplit1; ++s) M = fmaxf(M, sm[hh * nsplit1 + s]);
+            float num = 0.0f, den = 0.0f;
+            if (M != -INFINITY) {
+                const float* ph = base + (size_t)hh * nsplit1 * kPartStride + 4 + tid;
+                int s = 0;
+                for (; s + 4 <= nsplit1; s += 4) {
+                    float o4[4], w4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float m = sm[hh * nsplit1 + s + u];
+                        w4[u] = (m == -INFINITY) ? 0.0f : ex2(m - M);
+                        o4[u] = (m == -INFINITY) ? 0.0f : __ldcg(ph + (size_t)(s + u) * kPartStride);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        num = fmaf(w4[u], o4[u], num);
+                        den = fmaf(w4[u], sl[hh * nsplit1 + s + u], den);
+                    }
+                }
+                for (; s < nsplit1; ++s) {
+                    const float m = sm[hh * nsplit1 + s];
+                    if (m == -INFINITY) continue;
+                    const float w = ex2(m - M);
+                    num = fmaf(w, __ldcg(ph + (size_t)s * kPartStride), num);
+                    den = fmaf(w, sl[hh * nsplit1 + s], den);
+                }
+            }
+            a.out[((size_t)b * a.hq + 4 * h + hh) * kD + tid] = (den > 0.0f) ? num / den : 0.0f;
         }
     }
-    a.out[((size_t)b * a.hq + j) * kD + d] = (den > 0.0f) ? num / den : 0.0f;
+}
+
+template <int FMT, int PM>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int L = a.seq_lens[b];
+    const int nsplit1 = a.nsplit + 1;
+    float* part = a.parts + ((size_t)(b * a.hq + 4 * h) * nsplit1 + split) * kPartStride;
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // pages past the block-table row are ignored (the header bounds L)
+    const int npages = min(max(0, L - kSink) / kPage, a.max_blocks);
+    const int p0 = (split - 1) * a.pages_per_split;
+    const int p1 = min(p0 + a.pages_per_split, npages);
+
+    if (split == 0) {
+        bf16_segment(a, b, h, L, part, smem);
+    } else if (p0 >= p1) {
+        if (threadIdx.x < 4) {
+            part[threadIdx.x * nsplit1 * kPartStride + 0] = -INFINITY;
+            part[threadIdx.x * nsplit1 * kPartStride + 1] = 0.0f;
+        }
+    } else {
+        const int n = p1 - p0;
+        constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(smem_u32(&ctl->full[s]), 1);
+                mbar_init(smem_u32(&ctl->empty[s]), 1);
+            }
+            ctl->abort_flag = 0;
+            ctl->issued = 0;
+            fence_mbar_init();
+        }
+        if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
+        __syncthreads();
+        if (warp == kConsumers) {
+            // ---------------------------------------------------- producer --
+            if (lane == 0) {
+                const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
+                int k = 0;
+                for (; k < n; ++k) {
+                    const int s = k % kStages;
+                    if (k >= kStages &&
+                        !mbar_wait_bounded(smem_u32(&ctl->empty[s]), ((k / kStages) - 1) & 1, kWaitLimitNs,
+                                           &ctl->abort_flag)) {
+                        if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+                        ctl->abort_flag = 1;
+                        break;
+                    }
+                    const int64_t phys = bt[k];
+                    const uint8_t* krec = a.pool + ((phys * a.hkv + h) * 2) * (int64_t)RB;
+                    const uint32_t full = smem_u32(&ctl->full[s]);
+                    const uint32_t dst = smem_u32(smem + s * kStageBytes);
+                    mbar_arrive_expect_tx(full, 2 * RB);
+                    bulk_g2s(dst, krec, RB, full);
+                    bulk_g2s(dst + kMaxRec, krec + RB, RB, full);
+                }
+                ctl->issued = k;
+            }
+            __syncthreads();   // (A)
+            // drain copies an aborted run left in flight before the ring is reused
+            if (lane == 0 && ctl->abort_flag) {
+                for (int kk = 0; kk < ctl->issued; ++kk)
+                    if (kk >= ctl->consumed[kk % kConsumers])
+                        (void)mbar_wait_bounded(smem_u32(&ctl->full[kk % kStages]), (kk / kStages) & 1,
+                                                kWaitLimitNs, nullptr);
+            }
+        } else {
+            consume_pages<FMT, PM>(a, b, h, n, smem, ctl, warp, lane);   // contains (A)
+        }
+        __syncthreads();   // (B) warp states and drained ring
+        write_split_partial(a, part, smem, ctl);
+    }
+
+    // ---------------- ticket: the last CTA of (b, h) merges all splits
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(&a.counters[b * a.hkv + h], 1);
+        ctl->is_last = (ticket == nsplit1 - 1);
+    }
+    __syncthreads();
+    if (ctl->is_last) {
+        __threadfence();
+        combine_splits(a, b, h, smem);
+        if (threadIdx.x == 0) a.counters[b * a.hkv + h] = 0;
+    }
 }
 
 // ------------------------------------------------------ bounded-wait test --
@@ -589,35 +668,62 @@ void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_s
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
             sms = 148;
     }
+    // two CTAs fit per SM; split 0 of every (sequence, kv head) is the BF16
+    // sink/tail CTA, so a single wave holds units * (splits + 1) CTAs
     const int slots = 2 * sms;
     const int units = max(1, B * hkv);
-    int ns = (slots + units - 1) / units;
+    int ns = max(1, slots / units - 1);
     ns = max(1, min(ns, max(1, max_blocks)));
     int pps = max(1, (max_blocks + ns - 1) / ns);
     ns = max(1, (max_blocks + pps - 1) / pps);
+    if (ns > kMaxSplits - 1) {
+        pps = (max_blocks + kMaxSplits - 2) / (kMaxSplits - 1);
+        ns = (max_blocks + pps - 1) / pps;
+    }
     *nsplit = ns;
     *pages_per_split = pps;
 }
 
+size_t decode_counter_bytes(int B, int hkv) { return ((size_t)B * hkv * sizeof(int) + 255) / 256 * 256; }
+
+size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit) {
+    return decode_counter_bytes(B, hkv) + (size_t)B * hq * (nsplit + 1) * kPartStride * sizeof(float);
+}
+
+using DecodeFn = void (*)(DecodeArgs);
+
+template <int FMT>
+DecodeFn pick_decode(int p_mode) {
+    if (p_mode == BD_P_NONE) return decode_kernel<FMT, BD_P_NONE>;
+    if (p_mode == BD_P_AMAX6) return decode_kernel<FMT, BD_P_AMAX6>;
+    return decode_kernel<FMT, BD_P_AMAX2_OR_AMAX6>;
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
-    static bool attr_set[2] = {false, false};
-    const int f = a.format;
-    auto kern = (f == BD_FORMAT_NVFP4) ? decode_kernel<BD_FORMAT_NVFP4> : decode_kernel<BD_FORMAT_MXFP4>;
-    if (!attr_set[f]) {
+    static bool attr_set[2][3] = {};
+    const int f = a.format, pm = a.p_mode;
+    DecodeFn kern = (f == BD_FORMAT_NVFP4) ? pick_decode<BD_FORMAT_NVFP4>(pm) : pick_decode<BD_FORMAT_MXFP4>(pm);
+    if (!attr_set[f][pm]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_set[f] = true;
+        attr_set[f][pm] = true;
     }
-    dim3 grid((unsigned)(a.nsplit + 1), (unsigned)a.hkv, (unsigned)a.B);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    combine_kernel<<<dim3((unsigned)a.hq, (unsigned)a.B), kD, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.nsplit + 1), (unsigned)a.hkv, (unsigned)a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s) {

@@ -105,6 +105,11 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float* x, f
 
 __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
     __shared__ float red[16];
+    // Programmatic dependent launch: wait for the grid that precedes us in the
+    // stream (its outputs may feed q), then let the dependent decode launch so
+    // that it can start streaming pages while this kernel runs.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.x;
     const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
     const int hq = a.hq;
@@ -202,8 +207,16 @@ __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
 
 cudaError_t launch_query(const QueryArgs& a, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
-    query_kernel<<<a.B, a.hq * 8, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.B);
+    cfg.blockDim = dim3((unsigned)(a.hq * 8));
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, query_kernel, a);
 }
 
 }  // namespace bd

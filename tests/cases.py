@@ -127,9 +127,8 @@ def run_gpu(c: Case, dev="cuda", stream=None, pool=None) -> dict:
     sl = torch.from_numpy(c.seq_lens).to(dev)
     sk, sv, tk, tv = g(c.sink_k), g(c.sink_v), g(c.tail_k), g(c.tail_v)
     out = torch.full((B, HQ, D), float("nan"), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(1, bd.decode_workspace_size(c.ctx, B, bt.shape[1])) // 4 + 1, dtype=torch.float32,
+    ws = torch.zeros(max(1, bd.decode_workspace_size(c.ctx, B, bt.shape[1])) // 4 + 1, dtype=torch.float32,
                      device=dev)
-    ws.fill_(float("nan"))
     bd.decode_attention(c.ctx, 0, qp, q, pool, bt, sl, sk, sv, tk, tv, c.spec.tau, c.gk, c.gv, out, ws, stream)
     torch.cuda.synchronize()
     res = dict(pool=pool.cpu().numpy(), qp=qp.cpu().numpy(), out=out.cpu().double().numpy())
