@@ -197,6 +197,35 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
                         float k_gscale, float v_gscale, float* out, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* bd_decode_attention without a caller workspace and without any device
+ * allocation.  No page of the method has a counterpart: this entry point
+ * exists for callers that cannot call cudaMalloc -- code that runs inside
+ * another framework's memory pool or allocator, a plugin that is handed only
+ * its input and output buffers, or a process whose GPU memory is reserved up
+ * front -- and so cannot provide the workspace bd_decode_attention needs.
+ * Arguments are those of bd_decode_attention minus ws / ws_bytes; inputs and
+ * out are still caller-owned device memory.
+ *  - The split tickets and split partials live in one fixed 4 MiB device
+ *    array inside the library (every GPU that loads the library holds it
+ *    until the process exits).  A call whose tickets and partials need more
+ *    (bd_decode_workspace_size(ctx, B, max_blocks) > 4 MiB) is rejected with
+ *    BD_ERR_WORKSPACE before anything is launched: use bd_decode_attention
+ *    with a workspace instead.
+ *  - Every call shares that array and clears its tickets on `stream` first;
+ *    calls that overlap on the GPU (other streams, other threads) race and
+ *    must be serialized by the caller.
+ *  - The first call on a device looks up the array's device address; make
+ *    that first call before capturing a stream into a CUDA graph.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.  A
+ *    bounded device wait that runs out is recorded in the context's error
+ *    word only if that word already exists (any other launch call or
+ *    bd_set_key_shift creates it); this call never creates it. */
+int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, const void* q,
+                                const void* kv_pool, const int32_t* block_table, int max_blocks,
+                                const int32_t* seq_lens, const void* sink_k, const void* sink_v,
+                                const void* tail_k, const void* tail_v, int B, float tau,
+                                float k_gscale, float v_gscale, float* out, void* stream);
+
 /* Synchronize `stream`, copy the context's device error word into *out
  * (BD_OK or BD_ERR_TIMEOUT) and reset it to BD_OK. */
 int bd_read_device_error(bd_ctx* ctx, void* stream, int* out);

@@ -44,7 +44,8 @@ def make_config(num_layers=1, num_q_heads=32, num_kv_heads=8, format=FORMAT_NVFP
 
 EXPORTS = ("bd_create", "bd_destroy", "bd_status_string", "bd_set_key_shift", "bd_record_bytes",
            "bd_query_packed_bytes", "bd_quantize_kv_pages", "bd_quantize_query", "bd_decode_workspace_size",
-           "bd_decode_attention", "bd_read_device_error", "bd_selftest_bounded_wait")
+           "bd_decode_attention", "bd_decode_attention_noalloc", "bd_read_device_error",
+           "bd_selftest_bounded_wait")
 
 _lib = None
 
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "bd_quantize_query": (I, [P, I, P, I, P, P]),
             "bd_decode_workspace_size": (SZ, [P, I, I]),
             "bd_decode_attention": (I, [P, I, P, P, P, P, I, P, P, P, P, P, I, F, F, F, P, P, SZ, P]),
+            "bd_decode_attention_noalloc": (I, [P, I, P, P, P, P, I, P, P, P, P, P, I, F, F, F, P, P]),
             "bd_read_device_error": (I, [P, P, ctypes.POINTER(I)]),
             "bd_selftest_bounded_wait": (I, [P, I, P]),
         }
@@ -182,6 +184,19 @@ def decode_attention(ctx: Context, layer: int, q_packed, q, kv_pool, block_table
                                      max_blocks, _ptr(seq_lens), _ptr(sink_k), _ptr(sink_v), _ptr(tail_k),
                                      _ptr(tail_v), B, tau, k_gscale, v_gscale, _ptr(out), _ptr(ws), ws_bytes,
                                      _stream(stream)), "bd_decode_attention")
+
+
+def decode_attention_noalloc(ctx: Context, layer: int, q_packed, q, kv_pool, block_table, seq_lens, sink_k, sink_v,
+                             tail_k, tail_v, tau: float, k_gscale: float, v_gscale: float, out, stream=None):
+    """bd_decode_attention_noalloc: the decode without a caller workspace and
+    without device allocation, for callers that cannot allocate GPU memory
+    (its scratch is a fixed 4 MiB array inside the library)."""
+    B = q.shape[0]
+    max_blocks = block_table.shape[1] if block_table is not None and block_table.dim() == 2 else 0
+    _check(lib().bd_decode_attention_noalloc(ctx.handle, layer, _ptr(q_packed), _ptr(q), _ptr(kv_pool),
+                                             _ptr(block_table), max_blocks, _ptr(seq_lens), _ptr(sink_k), _ptr(sink_v),
+                                             _ptr(tail_k), _ptr(tail_v), B, tau, k_gscale, v_gscale, _ptr(out),
+                                             _stream(stream)), "bd_decode_attention_noalloc")
 
 
 def read_device_error(ctx: Context, stream=None) -> int:

@@ -215,6 +215,63 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     return cuda_status(bd::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, const void* q, const void* kv_pool,
+                                const int32_t* block_table, int max_blocks, const int32_t* seq_lens,
+                                const void* sink_k, const void* sink_v, const void* tail_k, const void* tail_v, int B,
+                                float tau, float k_gscale, float v_gscale, float* out, void* stream) {
+    // Same checks as bd_decode_attention; no cudaMalloc, cudaFree or other
+    // allocating call is made on this path.
+    if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers || B < 0 || B > (1 << 20)) return BD_ERR_INVALID_ARG;
+    if (max_blocks < 0 || max_blocks > (1 << 22)) return BD_ERR_INVALID_ARG;
+    if (!finite_in(tau, 0.0f, 448.0f)) return BD_ERR_INVALID_ARG;
+    if (!finite_in(k_gscale, 1e-30f, 1e30f) || !finite_in(v_gscale, 1e-30f, 1e30f)) return BD_ERR_INVALID_ARG;
+    if (B == 0) return BD_OK;
+    if (!q_packed || !q || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v || !out) return BD_ERR_INVALID_ARG;
+    if (max_blocks > 0 && (!block_table || !kv_pool)) return BD_ERR_INVALID_ARG;
+    const uintptr_t align = (uintptr_t)q_packed | (uintptr_t)kv_pool | (uintptr_t)q | (uintptr_t)sink_k |
+                            (uintptr_t)sink_v | (uintptr_t)tail_k | (uintptr_t)tail_v | (uintptr_t)out;
+    if (align & 15u) return BD_ERR_INVALID_ARG;
+    // the fixed scratch must hold this call's tickets and split partials
+    const size_t need = bd_decode_workspace_size(ctx, B, max_blocks);
+    if (need > bd::kNoAllocScratchBytes) return BD_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (bd::noalloc_scratch(&scratch) != cudaSuccess) return BD_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t counter_bytes = bd::decode_counter_bytes(B, ctx->cfg.num_kv_heads);
+    // the tickets must start at zero
+    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return BD_ERR_CUDA;
+    bd::DecodeArgs a;
+    a.qp = static_cast<const uint8_t*>(q_packed);
+    a.q = static_cast<const uint16_t*>(q);
+    a.pool = static_cast<const uint8_t*>(kv_pool);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.sink_k = static_cast<const uint16_t*>(sink_k);
+    a.sink_v = static_cast<const uint16_t*>(sink_v);
+    a.tail_k = static_cast<const uint16_t*>(tail_k);
+    a.tail_v = static_cast<const uint16_t*>(tail_v);
+    a.out = out;
+    a.counters = static_cast<int*>(scratch);
+    a.parts = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + counter_bytes);
+    // a bounded wait that runs out is recorded only if the context already
+    // has its device error word (this path never creates it)
+    a.err = ctx->d_err;
+    a.qstride = bd::qpack_stride(ctx->cfg.num_q_heads);
+    a.B = B;
+    a.hq = ctx->cfg.num_q_heads;
+    a.hkv = ctx->cfg.num_kv_heads;
+    a.max_blocks = max_blocks;
+    bd::decode_splits(B, a.hkv, max_blocks, &a.nsplit, &a.pages_per_split);
+    a.format = ctx->cfg.format;
+    a.centering = ctx->cfg.centering;
+    a.p_mode = ctx->cfg.p_mode;
+    a.p_c = ctx->cfg.p_c;
+    a.tau = tau;
+    a.gk = k_gscale;
+    a.gv = v_gscale;
+    return cuda_status(bd::launch_decode(a, s));
+}
+
 int bd_read_device_error(bd_ctx* ctx, void* stream, int* out) {
     if (!ctx || !out) return BD_ERR_INVALID_ARG;
     if (!ctx->d_err) {

@@ -43,6 +43,8 @@
 // packed or raw query first waits on the preceding grid.
 #include <math.h>
 
+#include <mutex>
+
 #include "bd_device.cuh"
 
 namespace bd {
@@ -724,6 +726,38 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// ------------------------------------------- fixed scratch (no allocation) --
+//
+// bd_decode_attention_noalloc serves callers that cannot call cudaMalloc --
+// for example code running inside another framework's memory pool, a plugin
+// that is handed only its input and output buffers, or a process whose GPU
+// memory is reserved up front.  Its split tickets and split partials live in
+// this file-scope array instead of a caller workspace.  Every GPU that loads
+// the library holds the array until the process exits; every call shares it,
+// so calls that overlap on the GPU race.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch(void** out) {
+    // In host code g_noalloc_scratch names a host-side stand-in, not device
+    // memory: the device address is looked up once per device, with that
+    // device current, and cached.
+    static std::mutex lock;
+    static void* addr[kMaxNoAllocDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxNoAllocDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(lock);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s) {

@@ -67,4 +67,9 @@ void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_s
 size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit);
 size_t decode_counter_bytes(int B, int hkv);
 
+// Fixed device scratch of bd_decode_attention_noalloc (see bd_decode.cu).
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
+constexpr int kMaxNoAllocDevices = 64;
+cudaError_t noalloc_scratch(void** out);
+
 }  // namespace bd
