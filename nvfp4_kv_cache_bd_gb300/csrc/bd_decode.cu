@@ -71,7 +71,8 @@ struct Ctl {
     int is_last;
 };
 constexpr int kScratchBytes = kConsumers * 8 * 2 * 32 * 4;   // per-warp score scratch
-constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes;
+constexpr int kPTabBytes = 2 * 128 * 4;                        // probability scale tables
+constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes + kPTabBytes;
 static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
 static_assert(sizeof(Ctl) % 16 == 0, "score scratch must stay 16-byte aligned");
 
@@ -276,7 +277,9 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + t] : 0.0f;
     const float ccf = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
     const float tau = a.tau;
-    const uint32_t inv_cc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / ccf)));
+    // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c) f16x2
+    const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
+    const uint32_t* ptab_sdc = reinterpret_cast<const uint32_t*>(ptab_rcp + 128);
     const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
     const int gs = g & 3;
 
@@ -329,16 +332,25 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     fk1 = pow2i(m1 - 127);
                 }
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t p0w = byte_pair(c0, kk), p1w = byte_pair(c1, kk);
-                    const uint32_t sa = kk < 4 ? s0lo : s0hi, sb2 = kk < 4 ? s1lo : s1hi;
+                for (int j = 0; j < 4; ++j) {
+                    // word j holds bytes 4j..4j+3: k-tiles 2j (bytes 4j, 4j+1) and 2j+1
+                    uint32_t f0[4], f1[4];
+                    e2m1x8_to_f16x2x4(cw0[j], f0);
+                    e2m1x8_to_f16x2x4(cw1[j], f1);
+                    const uint32_t sa = j < 2 ? s0lo : s0hi, sb2 = j < 2 ? s1lo : s1hi;
                     uint32_t A[4];
-                    A[0] = hmul2(e2m1x2_to_f16x2(p0w & 0xFF), sa);
-                    A[1] = hmul2(e2m1x2_to_f16x2(p1w & 0xFF), sb2);
-                    A[2] = hmul2(e2m1x2_to_f16x2(p0w >> 8), sa);
-                    A[3] = hmul2(e2m1x2_to_f16x2(p1w >> 8), sb2);
-                    mma16816(acc, A, qB[2 * kk], qB[2 * kk + 1]);
+                    A[0] = hmul2(f0[0], sa);
+                    A[1] = hmul2(f1[0], sb2);
+                    A[2] = hmul2(f0[1], sa);
+                    A[3] = hmul2(f1[1], sb2);
+                    mma16816(acc, A, qB[4 * j], qB[4 * j + 1]);
+                    A[0] = hmul2(f0[2], sa);
+                    A[1] = hmul2(f1[2], sb2);
+                    A[2] = hmul2(f0[3], sa);
+                    A[3] = hmul2(f1[3], sb2);
+                    mma16816(acc, A, qB[4 * j + 2], qB[4 * j + 3]);
                 }
                 const float s0 = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
                 const float s1 = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
@@ -396,12 +408,12 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 16));
                     const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (am < tau);
                     const float sv = two ? am * 0.5f : __fdiv_rn(am, 6.0f);
-                    const uint32_t sdh = e4m3x2_to_f16x2(e4m3(sv));
-                    const float sd = __half2float(__ushort_as_half((unsigned short)(sdh & 0xFFFF)));
-                    const float inv = __frcp_rn(sd);
-                    const bool zero = (sd == 0.0f) || isinf(inv);
-                    const uint32_t byte = zero ? 0u : e2m1x2(__fmul_rn(u0, inv), __fmul_rn(u1, inv));
-                    pv = hmul2(e2m1x2_to_f16x2(byte), hmul2(bcast_lo(sdh), inv_cc));
+                    // scale byte -> 1/sd (correctly rounded) and (sd/c, sd/c) from the tables;
+                    // byte 0 is the zero scale (S == 0: all codes zero)
+                    const uint32_t sbyte = e4m3(sv);
+                    const float inv = ptab_rcp[sbyte];
+                    const uint32_t byte = (sbyte == 0) ? 0u : e2m1x2(__fmul_rn(u0, inv), __fmul_rn(u1, inv));
+                    pv = hmul2(e2m1x2_to_f16x2(byte), ptab_sdc[sbyte]);
                 }
                 uint32_t b01 = __shfl_sync(kFull, pv, 4 * t + gs);
                 uint32_t b23 = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
@@ -418,15 +430,24 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     vs0 = f16_pow2((int)(e0 & 0xFF) - ev_ref) | (f16_pow2((int)(e0 >> 8) - ev_ref) << 16);
                     vs1 = f16_pow2((int)(e1 & 0xFF) - ev_ref) | (f16_pow2((int)(e1 >> 8) - ev_ref) << 16);
                 }
+                const uint32_t vw0[4] = {v0.x, v0.y, v0.z, v0.w}, vw1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int bm = 0; bm < 8; ++bm) {
-                    const uint32_t w0 = byte_pair(v0, bm), w1 = byte_pair(v1, bm);
+                for (int j = 0; j < 4; ++j) {
+                    // word j holds dims 16g+4j .. 16g+4j+3: m-tiles 2j (dims 4j, 4j+1) and 2j+1
+                    uint32_t f0[4], f1[4];
+                    e2m1x8_to_f16x2x4(vw0[j], f0);
+                    e2m1x8_to_f16x2x4(vw1[j], f1);
                     uint32_t A[4];
-                    A[0] = hmul2(e2m1x2_to_f16x2(w0 & 0xFF), vs0);
-                    A[1] = hmul2(e2m1x2_to_f16x2(w0 >> 8), vs0);
-                    A[2] = hmul2(e2m1x2_to_f16x2(w1 & 0xFF), vs1);
-                    A[3] = hmul2(e2m1x2_to_f16x2(w1 >> 8), vs1);
-                    mma16816(op[bm], A, b01, b23);
+                    A[0] = hmul2(f0[0], vs0);
+                    A[1] = hmul2(f0[1], vs0);
+                    A[2] = hmul2(f1[0], vs1);
+                    A[3] = hmul2(f1[1], vs1);
+                    mma16816(op[2 * j], A, b01, b23);
+                    A[0] = hmul2(f0[2], vs0);
+                    A[1] = hmul2(f0[3], vs0);
+                    A[2] = hmul2(f1[2], vs1);
+                    A[3] = hmul2(f1[3], vs1);
+                    mma16816(op[2 * j + 1], A, b01, b23);
                 }
             }
         }
@@ -509,53 +530,72 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
     }
 }
 
-// Merge every split of (b, kv head h) into out (run by the last CTA).
+// Merge every split of (b, kv head h) into out (run by the last CTA).  Each
+// of 128 threads owns 4 consecutive dims of one head and keeps 8 independent
+// 16-byte partial loads in flight, so the merge costs a few memory round
+// trips rather than one per split.
 __device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem) {
     const int nsplit1 = a.nsplit + 1;
-    float* sm = reinterpret_cast<float*>(smem);            // [4][nsplit1] m
-    float* sl = sm + 4 * nsplit1;                          // [4][nsplit1] l
+    float* sw = reinterpret_cast<float*>(smem);            // [4][nsplit1] weights 2^(m - M)
+    float* sl = sw + 4 * nsplit1;                          // [4][nsplit1] l
+    float* sM = sl + 4 * nsplit1;                          // [4] max
     const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
-    for (int i = threadIdx.x; i < 4 * nsplit1; i += blockDim.x) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 4 * nsplit1; i += blockDim.x) {
         const float* p = base + (size_t)i * kPartStride;   // i = hh * nsplit1 + s
         const float l = __ldcg(p + 1);
         sl[i] = l;
-        sm[i] = (l > 0.0f) ? __ldcg(p) : -INFINITY;
+        sw[i] = (l > 0.0f) ? __ldcg(p) : -INFINITY;
     }
     __syncthreads();
-    const int tid = threadIdx.x;
+    if (tid < 4) {
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit1; ++s) M = fmaxf(M, sw[tid * nsplit1 + s]);
+        sM[tid] = M;
+    }
+    __syncthreads();
+    for (int i = tid; i < 4 * nsplit1; i += blockDim.x) {
+        const float M = sM[i / nsplit1];
+        sw[i] = (sw[i] == -INFINITY) ? 0.0f : ex2(sw[i] - M);
+    }
+    __syncthreads();
     if (tid < kD) {
-#pragma unroll 1
-        for (int hh = 0; hh < 4; ++hh) {
-            float M = -INFINITY;
-            for (int s = 0; s < nsplit1; ++s) M = fmaxf(M, sm[hh * nsplit1 + s]);
-            float num = 0.0f, den = 0.0f;
-            if (M != -INFINITY) {
-                const float* ph = base + (size_t)hh * nsplit1 * kPartStride + 4 + tid;
-                int s = 0;
-                for (; s + 4 <= nsplit1; s += 4) {
-                    float o4[4], w4[4];
+        const int hh = tid >> 5, d0 = (tid & 31) * 4;
+        const float* ph = base + (size_t)hh * nsplit1 * kPartStride + 4 + d0;
+        const float* w = sw + hh * nsplit1;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.0f;
+        int s = 0;
+        for (; s + 8 <= nsplit1; s += 8) {
+            float4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float m = sm[hh * nsplit1 + s + u];
-                        w4[u] = (m == -INFINITY) ? 0.0f : ex2(m - M);
-                        o4[u] = (m == -INFINITY) ? 0.0f : __ldcg(ph + (size_t)(s + u) * kPartStride);
-                    }
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(ph + (size_t)(s + u) * kPartStride));
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        num = fmaf(w4[u], o4[u], num);
-                        den = fmaf(w4[u], sl[hh * nsplit1 + s + u], den);
-                    }
-                }
-                for (; s < nsplit1; ++s) {
-                    const float m = sm[hh * nsplit1 + s];
-                    if (m == -INFINITY) continue;
-                    const float w = ex2(m - M);
-                    num = fmaf(w, __ldcg(ph + (size_t)s * kPartStride), num);
-                    den = fmaf(w, sl[hh * nsplit1 + s], den);
+            for (int u = 0; u < 8; ++u) {
+                const float wu = w[s + u];
+                if (wu != 0.0f) {
+                    num.x = fmaf(wu, v[u].x, num.x);
+                    num.y = fmaf(wu, v[u].y, num.y);
+                    num.z = fmaf(wu, v[u].z, num.z);
+                    num.w = fmaf(wu, v[u].w, num.w);
+                    den = fmaf(wu, sl[hh * nsplit1 + s + u], den);
                 }
             }
-            a.out[((size_t)b * a.hq + 4 * h + hh) * kD + tid] = (den > 0.0f) ? num / den : 0.0f;
         }
+        for (; s < nsplit1; ++s) {
+            const float wu = w[s];
+            if (wu == 0.0f) continue;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(ph + (size_t)s * kPartStride));
+            num.x = fmaf(wu, v.x, num.x);
+            num.y = fmaf(wu, v.y, num.y);
+            num.z = fmaf(wu, v.z, num.z);
+            num.w = fmaf(wu, v.w, num.w);
+            den = fmaf(wu, sl[hh * nsplit1 + s], den);
+        }
+        const float r = (den > 0.0f) ? 1.0f / den : 0.0f;
+        float4 o = make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
+        if (!(den > 0.0f)) o = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(a.out + ((size_t)b * a.hq + 4 * h + hh) * kD + d0) = o;
     }
 }
 
@@ -594,6 +634,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             fence_mbar_init();
         }
         if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
+        if (threadIdx.x < 128) {
+            // exact per-byte tables of the probability quantizer for the E4M3
+            // scale byte bb: the correctly rounded 1/sd, and (sd/c, sd/c) as f16x2
+            float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
+            const uint32_t bb = threadIdx.x;
+            const float sd = e4m3_value(bb);
+            const float cc = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
+            tab[bb] = (bb == 0) ? 0.0f : __frcp_rn(sd);
+            const uint32_t sdh = e4m3x2_to_f16x2(bb);
+            const uint32_t icc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / cc)));
+            reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
+        }
         __syncthreads();
         if (warp == kConsumers) {
             // ---------------------------------------------------- producer --

@@ -36,6 +36,17 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
     return r;
 }
 
+// Four bytes of E2M1 code pairs (one 32-bit word) -> four f16x2: byte j
+// goes to o[j], its low nibble to the low half.  The word is split into its
+// bytes with a vector mov so no shift/mask is spent per byte.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* o) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
 // Binary32 -> E4M3 byte, round to nearest even, saturating at 448.
 __device__ __forceinline__ uint32_t e4m3(float s) {
     uint16_t r;
