@@ -67,6 +67,7 @@ struct Ctl {
     float wl[kConsumers][4];   // per-warp softmax denominator per head
     int abort_flag;
     int issued;
+    int stage_page[kStages];   // page index the stage's latest fill holds (-1: none)
     int consumed[kConsumers];  // first page index each warp did not consume
     int is_last;
 };
@@ -103,6 +104,34 @@ __device__ __forceinline__ uint32_t f16_pow2(int k) {
     if (k >= -14) return (uint32_t)(k + 15) << 10;
     if (k >= -24) return 1u << (k + 24);
     return 0u;
+}
+
+__device__ __forceinline__ int ld_acquire_shared(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_shared(int* p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// Wait until the stage holds page `page` and its full barrier has completed
+// the phase of the given parity (bounded like mbar_wait_bounded).  The tag is
+// read first: the producer publishes it only after the stage's previous fill
+// completed and was released, so once the tag matches, the parity test can
+// no longer confuse the awaited phase with the one two fills earlier.
+__device__ __forceinline__ bool wait_stage_page(uint32_t bar, uint32_t parity, const int* tag, int page,
+                                                const volatile int* abort_flag) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_shared(tag) == page && mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u) {
+            if (abort_flag && *abort_flag) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kWaitLimitNs) return false;
+        }
+    }
 }
 
 // ------------------------------------------------------ BF16 sink + tail --
@@ -292,7 +321,11 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     int k = warp;
     for (; k < n; k += kConsumers) {
         const int s = k % kStages;
-        if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), (k / kStages) & 1, kWaitLimitNs, &ctl->abort_flag)) {
+        // Warps take pages round-robin from a 5-stage ring, so a warp may start
+        // waiting for fill j of a stage before fill j-1 has landed; the phase
+        // parity alone cannot tell fill j-2 from fill j, the page tag can.
+        if (!wait_stage_page(smem_u32(&ctl->full[s]), (k / kStages) & 1, &ctl->stage_page[s], k,
+                             &ctl->abort_flag)) {
             if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
             ctl->abort_flag = 1;
             break;
@@ -631,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             }
             ctl->abort_flag = 0;
             ctl->issued = 0;
+            for (int st = 0; st < kStages; ++st) ctl->stage_page[st] = -1;
             fence_mbar_init();
         }
         if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
@@ -665,6 +699,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                     const uint8_t* krec = a.pool + ((phys * a.hkv + h) * 2) * (int64_t)RB;
                     const uint32_t full = smem_u32(&ctl->full[s]);
                     const uint32_t dst = smem_u32(smem + s * kStageBytes);
+                    // tag the fill before it is armed: consumers accept a completed
+                    // phase only together with their own page index
+                    st_release_shared(&ctl->stage_page[s], k);
                     mbar_arrive_expect_tx(full, 2 * RB);
                     bulk_g2s(dst, krec, RB, full);
                     bulk_g2s(dst + kMaxRec, krec + RB, RB, full);
