@@ -57,7 +57,7 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMaxRec = 9216;
 constexpr int kStageBytes = 2 * kMaxRec;
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kMaxSplits = 1024;
+constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages 4 x 43 partials
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 struct Ctl {
@@ -72,10 +72,11 @@ struct Ctl {
     int is_last;
 };
 constexpr int kScratchBytes = kConsumers * 8 * 2 * 32 * 4;   // per-warp score scratch
-constexpr int kPTabBytes = 2 * 128 * 4;                        // probability scale tables
+constexpr int kPTabBytes = 3 * 128 * 4;                        // scale tables (see decode_kernel)
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes + kPTabBytes;
 static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
 static_assert(sizeof(Ctl) % 16 == 0, "score scratch must stay 16-byte aligned");
+static_assert(4 * kMaxSplits * kPartStride * 4 <= kRingBytes, "the combine stages a head group's partials in the ring");
 
 __device__ __forceinline__ float ex2(float x) {
     float r;
@@ -134,6 +135,19 @@ __device__ __forceinline__ bool wait_stage_page(uint32_t bar, uint32_t parity, c
     }
 }
 
+// a / 6 correctly rounded.  For a >= 2^-100, Markstein's method for division
+// by a constant: q0 = a * RN(1/6), the exact remainder r = a - 6 q0 by one
+// FMA, and one more FMA q0 + r * RN(1/6) (valid while nothing underflows);
+// smaller a takes the IEEE division.  Checked bit for bit against __fdiv_rn
+// for every binary32 a in (0, 8] (the probability block maxima).
+__device__ __forceinline__ float div6(float a) {
+    if (a < 7.888609052210118e-31f) return __fdiv_rn(a, 6.0f);   // 2^-100
+    const float y = 1.0f / 6.0f;
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, 6.0f, a);
+    return __fmaf_rn(r, y, q0);
+}
+
 // ------------------------------------------------------ BF16 sink + tail --
 
 // Shared-memory row pitch of a staged bf16 head vector: 256 B plus 16 B so
@@ -149,6 +163,8 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
     const int T = ns + nt;
     const int nsplit1 = a.nsplit + 1;
     const int tid = threadIdx.x;
+    // the sink/tail rows and q may be produced by the preceding grid
+    griddep_wait();
     if (T == 0) {
         if (tid < 4) {
             part[tid * nsplit1 * kPartStride + 0] = -INFINITY;
@@ -174,7 +190,6 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
         cp_async16(smem_u32(vs + tau * kRowPitch + 16 * c), vb);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    griddep_wait();
     if (tid < 4 * kD / 8) {
         const int hh = tid >> 4, c = tid & 15;
         const uint4 u = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.hq + 4 * h + hh) * kD + 8 * c);
@@ -306,9 +321,11 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + t] : 0.0f;
     const float ccf = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
     const float tau = a.tau;
-    // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c) f16x2
+    // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c)
+    // f16x2, [256,384) (sd, sd) f16x2
     const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
     const uint32_t* ptab_sdc = reinterpret_cast<const uint32_t*>(ptab_rcp + 128);
+    const uint32_t* ptab_sbc = reinterpret_cast<const uint32_t*>(ptab_rcp + 256);
     const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
     const int gs = g & 3;
 
@@ -333,13 +350,13 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         const uint8_t* Ks = smem + s * kStageBytes;
         const uint8_t* Vs = Ks + kMaxRec;
 
-        // ---------------- QK, two 16-token blocks per iteration: log2-scaled
+        // ---------------- QK, four 16-token blocks per iteration: log2-scaled
         // scores of head t for tokens 16mi+g and 16mi+g+8 go to the scratch
         float mp = -INFINITY;
 #pragma unroll 1
-        for (int m2 = 0; m2 < 8; m2 += 2) {
+        for (int m2 = 0; m2 < 8; m2 += 4) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int mi = m2 + u;
                 const int tok0 = 16 * mi + g, tok1 = tok0 + 8;
                 const uint4 c0 = lds128(Ks + tok0 * 64 + 16 * t);
@@ -347,12 +364,13 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                 uint32_t s0lo, s0hi, s1lo, s1hi;
                 float fk0 = 1.0f, fk1 = 1.0f;
                 if (FMT == BD_FORMAT_NVFP4) {
-                    const uint32_t sd0 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok0 * 8 + 2 * t));
-                    const uint32_t sd1 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok1 * 8 + 2 * t));
-                    s0lo = bcast_lo(sd0);
-                    s0hi = bcast_hi(sd0);
-                    s1lo = bcast_lo(sd1);
-                    s1hi = bcast_hi(sd1);
+                    // (sd, sd) f16x2 of blocks 2t, 2t+1 of both rows from the table
+                    const uint8_t* sc0 = Ks + kCodeBytes + tok0 * 8 + 2 * t;
+                    const uint8_t* sc1 = Ks + kCodeBytes + tok1 * 8 + 2 * t;
+                    s0lo = ptab_sbc[sc0[0]];
+                    s0hi = ptab_sbc[sc0[1]];
+                    s1lo = ptab_sbc[sc1[0]];
+                    s1hi = ptab_sbc[sc1[1]];
                 } else {
                     const int e0 = Ks[kCodeBytes + tok0 * 4 + t], e1 = Ks[kCodeBytes + tok1 * 4 + t];
                     int m0 = max(e0, __shfl_xor_sync(kFull, e0, 1));
@@ -364,7 +382,8 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     fk0 = pow2i(m0 - 127);
                     fk1 = pow2i(m1 - 127);
                 }
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                // two accumulators halve the dependent MMA chain of the block
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
                 const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -383,8 +402,10 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     A[1] = hmul2(f1[2], sb2);
                     A[2] = hmul2(f0[3], sa);
                     A[3] = hmul2(f1[3], sb2);
-                    mma16816(acc, A, qB[4 * j + 2], qB[4 * j + 3]);
+                    mma16816(acc2, A, qB[4 * j + 2], qB[4 * j + 3]);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
                 const float s0 = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
                 const float s1 = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
                 sS[(2 * mi) * 32 + lane] = s0;
@@ -417,15 +438,39 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         }
 
         // ---------------- per 16-token block: probabilities, their FP4
-        // quantization, and P V into O_p^T[dims][heads]
+        // quantization, and P V.  NVFP4: the running max is updated first and
+        // the page weight 2^(m_p - M) is folded into the f16 Phat operand, so
+        // P V accumulates straight into O (one f16 rounding, < 2^-11
+        // relative, per weighted Phat).  MXFP4 keeps a per-page O_p because
+        // its V reference exponent changes from page to page.
+        const float mnt = fmaxf(Mt, mp);
+        const float wpage = ex2(mp - mnt);
+        uint32_t wh = 0x3C003C00u;   // (1, 1)
         float op[8][4];
+        if (FMT == BD_FORMAT_NVFP4) {
+            const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
+            const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
+            if (__any_sync(kFull, (aA != 1.0f) | (aB != 1.0f))) {
 #pragma unroll
-        for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
+                for (int bm = 0; bm < 8; ++bm) {
+                    o[bm][0] *= aA;
+                    o[bm][1] *= aB;
+                    o[bm][2] *= aA;
+                    o[bm][3] *= aB;
+                }
+            }
+            MA = mnA;
+            MB = mnB;
+            wh = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(wpage)));
+        } else {
+#pragma unroll
+            for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
+        }
         float lpage = 0.0f;
 #pragma unroll 1
-        for (int i2 = 0; i2 < 8; i2 += 2) {
+        for (int i2 = 0; i2 < 8; i2 += 4) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int i = i2 + u;
                 const float p0 = ex2(sS[(2 * i) * 32 + lane] - mp), p1 = ex2(sS[(2 * i + 1) * 32 + lane] - mp);
                 lpage += p0 + p1;
@@ -440,7 +485,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 8));
                     am = fmaxf(am, __shfl_xor_sync(kFull, am, 16));
                     const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (am < tau);
-                    const float sv = two ? am * 0.5f : __fdiv_rn(am, 6.0f);
+                    const float sv = two ? am * 0.5f : div6(am);
                     // scale byte -> 1/sd (correctly rounded) and (sd/c, sd/c) from the tables;
                     // byte 0 is the zero scale (S == 0: all codes zero)
                     const uint32_t sbyte = e4m3(sv);
@@ -448,9 +493,11 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     const uint32_t byte = (sbyte == 0) ? 0u : e2m1x2(__fmul_rn(u0, inv), __fmul_rn(u1, inv));
                     pv = hmul2(e2m1x2_to_f16x2(byte), ptab_sdc[sbyte]);
                 }
-                uint32_t b01 = __shfl_sync(kFull, pv, 4 * t + gs);
-                uint32_t b23 = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
-                if (g >= 4) b01 = b23 = 0u;
+                if (FMT == BD_FORMAT_NVFP4) pv = hmul2(pv, wh);
+                // lanes with g >= 4 feed the padding columns 4..7 (duplicates of
+                // heads 0..3); their outputs are never read
+                const uint32_t b01 = __shfl_sync(kFull, pv, 4 * t + gs);
+                const uint32_t b23 = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
                 const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * g);
                 const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * g);
                 uint32_t vs0, vs1;
@@ -475,12 +522,12 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     A[1] = hmul2(f0[1], vs0);
                     A[2] = hmul2(f1[0], vs1);
                     A[3] = hmul2(f1[1], vs1);
-                    mma16816(op[2 * j], A, b01, b23);
+                    mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j] : op[2 * j], A, b01, b23);
                     A[0] = hmul2(f0[2], vs0);
                     A[1] = hmul2(f0[3], vs0);
                     A[2] = hmul2(f1[2], vs1);
                     A[3] = hmul2(f1[3], vs1);
-                    mma16816(op[2 * j + 1], A, b01, b23);
+                    mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j + 1] : op[2 * j + 1], A, b01, b23);
                 }
             }
         }
@@ -489,22 +536,21 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
 
         // ---------------- merge the page into the warp's running state
-        {
-            const float mn = fmaxf(Mt, mp);
-            lacc = fmaf(lacc, ex2(Mt - mn), ex2(mp - mn) * lpage);
-            Mt = mn;
-        }
-        const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
-        const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
-        const float bA = ex2(mpA - mnA) * gV * fv, bB = ex2(mpB - mnB) * gV * fv;
-        MA = mnA;
-        MB = mnB;
+        lacc = fmaf(lacc, ex2(Mt - mnt), wpage * lpage);
+        Mt = mnt;
+        if (FMT == BD_FORMAT_MXFP4) {
+            const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
+            const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
+            const float bA = ex2(mpA - mnA) * fv, bB = ex2(mpB - mnB) * fv;
+            MA = mnA;
+            MB = mnB;
 #pragma unroll
-        for (int bm = 0; bm < 8; ++bm) {
-            o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
-            o[bm][1] = fmaf(o[bm][1], aB, bB * op[bm][1]);
-            o[bm][2] = fmaf(o[bm][2], aA, bA * op[bm][2]);
-            o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
+            for (int bm = 0; bm < 8; ++bm) {
+                o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
+                o[bm][1] = fmaf(o[bm][1], aB, bB * op[bm][1]);
+                o[bm][2] = fmaf(o[bm][2], aA, bA * op[bm][2]);
+                o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
+            }
         }
         __syncwarp();   // the scratch is rewritten by the next page
     }
@@ -517,10 +563,10 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
 #pragma unroll
         for (int bm = 0; bm < 8; ++bm) {
             const int d = 16 * g + 2 * bm;
-            sO[(warp * 4 + 2 * t) * kD + d] = o[bm][0];
-            sO[(warp * 4 + 2 * t + 1) * kD + d] = o[bm][1];
-            sO[(warp * 4 + 2 * t) * kD + d + 1] = o[bm][2];
-            sO[(warp * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3];
+            sO[(warp * 4 + 2 * t) * kD + d] = o[bm][0] * gV;
+            sO[(warp * 4 + 2 * t + 1) * kD + d] = o[bm][1] * gV;
+            sO[(warp * 4 + 2 * t) * kD + d + 1] = o[bm][2] * gV;
+            sO[(warp * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3] * gV;
         }
     }
     lacc += __shfl_xor_sync(kFull, lacc, 4);
@@ -563,72 +609,44 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
     }
 }
 
-// Merge every split of (b, kv head h) into out (run by the last CTA).  Each
-// of 128 threads owns 4 consecutive dims of one head and keeps 8 independent
-// 16-byte partial loads in flight, so the merge costs a few memory round
-// trips rather than one per split.
+// Merge every split of (b, kv head h) into out (run by the last CTA).  The
+// head group's partials are first staged into shared memory with one burst
+// of asynchronous 16-byte copies (a single memory round trip), then each of
+// 128 threads merges 4 consecutive dims of one head.
 __device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem) {
     const int nsplit1 = a.nsplit + 1;
-    float* sw = reinterpret_cast<float*>(smem);            // [4][nsplit1] weights 2^(m - M)
-    float* sl = sw + 4 * nsplit1;                          // [4][nsplit1] l
-    float* sM = sl + 4 * nsplit1;                          // [4] max
-    const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
     const int tid = threadIdx.x;
-    for (int i = tid; i < 4 * nsplit1; i += blockDim.x) {
-        const float* p = base + (size_t)i * kPartStride;   // i = hh * nsplit1 + s
-        const float l = __ldcg(p + 1);
-        sl[i] = l;
-        sw[i] = (l > 0.0f) ? __ldcg(p) : -INFINITY;
-    }
-    __syncthreads();
-    if (tid < 4) {
-        float M = -INFINITY;
-        for (int s = 0; s < nsplit1; ++s) M = fmaxf(M, sw[tid * nsplit1 + s]);
-        sM[tid] = M;
-    }
-    __syncthreads();
-    for (int i = tid; i < 4 * nsplit1; i += blockDim.x) {
-        const float M = sM[i / nsplit1];
-        sw[i] = (sw[i] == -INFINITY) ? 0.0f : ex2(sw[i] - M);
-    }
+    const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
+    float* sp = reinterpret_cast<float*>(smem);                 // [4][nsplit1][132] staged partials
+    const int nvec = 4 * nsplit1 * (kPartStride / 4);           // 16-byte pieces
+    for (int i = tid; i < nvec; i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (tid < kD) {
         const int hh = tid >> 5, d0 = (tid & 31) * 4;
-        const float* ph = base + (size_t)hh * nsplit1 * kPartStride + 4 + d0;
-        const float* w = sw + hh * nsplit1;
+        const float* ph = sp + (size_t)hh * nsplit1 * kPartStride;
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit1; ++s)
+            if (ph[s * kPartStride + 1] > 0.0f) M = fmaxf(M, ph[s * kPartStride]);
         float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
         float den = 0.0f;
-        int s = 0;
-        for (; s + 8 <= nsplit1; s += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(ph + (size_t)(s + u) * kPartStride));
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float wu = w[s + u];
-                if (wu != 0.0f) {
-                    num.x = fmaf(wu, v[u].x, num.x);
-                    num.y = fmaf(wu, v[u].y, num.y);
-                    num.z = fmaf(wu, v[u].z, num.z);
-                    num.w = fmaf(wu, v[u].w, num.w);
-                    den = fmaf(wu, sl[hh * nsplit1 + s + u], den);
-                }
+        if (M != -INFINITY) {
+            for (int s = 0; s < nsplit1; ++s) {
+                const float* p = ph + s * kPartStride;
+                if (!(p[1] > 0.0f)) continue;
+                const float w = ex2(p[0] - M);
+                const float4 v = *reinterpret_cast<const float4*>(p + 4 + d0);
+                num.x = fmaf(w, v.x, num.x);
+                num.y = fmaf(w, v.y, num.y);
+                num.z = fmaf(w, v.z, num.z);
+                num.w = fmaf(w, v.w, num.w);
+                den = fmaf(w, p[1], den);
             }
         }
-        for (; s < nsplit1; ++s) {
-            const float wu = w[s];
-            if (wu == 0.0f) continue;
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(ph + (size_t)s * kPartStride));
-            num.x = fmaf(wu, v.x, num.x);
-            num.y = fmaf(wu, v.y, num.y);
-            num.z = fmaf(wu, v.z, num.z);
-            num.w = fmaf(wu, v.w, num.w);
-            den = fmaf(wu, sl[hh * nsplit1 + s], den);
-        }
         const float r = (den > 0.0f) ? 1.0f / den : 0.0f;
-        float4 o = make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
-        if (!(den > 0.0f)) o = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(a.out + ((size_t)b * a.hq + 4 * h + hh) * kD + d0) = o;
+        *reinterpret_cast<float4*>(a.out + ((size_t)b * a.hq + 4 * h + hh) * kD + d0) =
+            make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
     }
 }
 
@@ -641,6 +659,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     float* part = a.parts + ((size_t)(b * a.hq + 4 * h) * nsplit1 + split) * kPartStride;
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Let the next kernel in the stream launch now: this kernel reads the
+    // query (and its sink/tail rows) and writes the workspace and out only
+    // after griddepcontrol.wait, so its producers can start streaming the
+    // layer's static FP4 pages while the previous grid still drains.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // pages past the block-table row are ignored (the header bounds L)
     const int npages = min(max(0, L - kSink) / kPage, a.max_blocks);
@@ -650,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     if (split == 0) {
         bf16_segment(a, b, h, L, part, smem);
     } else if (p0 >= p1) {
+        griddep_wait();
         if (threadIdx.x < 4) {
             part[threadIdx.x * nsplit1 * kPartStride + 0] = -INFINITY;
             part[threadIdx.x * nsplit1 * kPartStride + 1] = 0.0f;
@@ -669,8 +693,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         }
         if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
         if (threadIdx.x < 128) {
-            // exact per-byte tables of the probability quantizer for the E4M3
-            // scale byte bb: the correctly rounded 1/sd, and (sd/c, sd/c) as f16x2
+            // exact per-byte tables for the E4M3 scale byte bb: the correctly
+            // rounded 1/sd and (sd/c, sd/c) for the probability quantizer, and
+            // (sd, sd) for widening key blocks; all f16x2 entries are exact
             float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
             const uint32_t bb = threadIdx.x;
             const float sd = e4m3_value(bb);
@@ -679,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             const uint32_t sdh = e4m3x2_to_f16x2(bb);
             const uint32_t icc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / cc)));
             reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
+            reinterpret_cast<uint32_t*>(tab)[256 + bb] = bcast_lo(sdh);
         }
         __syncthreads();
         if (warp == kConsumers) {
@@ -724,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     }
 
     // ---------------- ticket: the last CTA of (b, h) merges all splits
+    griddep_wait();
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();

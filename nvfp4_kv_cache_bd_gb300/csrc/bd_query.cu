@@ -105,11 +105,12 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float* x, f
 
 __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
     __shared__ float red[16];
-    // Programmatic dependent launch: wait for the grid that precedes us in the
-    // stream (its outputs may feed q), then let the dependent decode launch so
-    // that it can start streaming pages while this kernel runs.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Programmatic dependent launch: let the dependent decode launch at once
+    // (it streams the layer's static FP4 pages and waits for this grid before
+    // it reads the packed query), then wait for the grid that precedes us in
+    // the stream, whose outputs may feed q.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int b = blockIdx.x;
     const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
     const int hq = a.hq;
