@@ -39,7 +39,7 @@ CTX = 131072
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--ctx", type=int, default=CTX)
@@ -66,36 +66,62 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = None
+        self.window = None
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t_end = time.time() + 10.0          # wait for the first sample before any timing starts
+        while time.time() < t_end and self._rows() == 0:
+            time.sleep(0.02)
+
+    def _rows(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def mark_begin(self):
+        """Called right before the timed region: rows from here on count."""
+        if self.proc is not None:
+            self.window = [self._rows(), None]
+
+    def mark_end(self):
+        """Called right after the timed region (after its synchronize)."""
+        if self.proc is not None and self.window is not None:
+            time.sleep(self.interval_ms / 1000.0)
+            self.window[1] = self._rows()
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        lines = open(self.path).read().splitlines()
+        os.unlink(self.path)
+        if self.window is not None:
+            lines = lines[self.window[0]:self.window[1]]
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
                 rows.append(parts)
-        os.unlink(self.path)
         if not rows:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -154,9 +180,10 @@ class DecodeWorkload:
                               device=device)
         self.bytes_per_layer = self.npages * HKV * 2 * self.rec
 
-    def layer(self, l, stream=None, q=None, ev=None):
+    def layer(self, l, stream=None, q=None, ev=None, out=None):
         bd = self.bd
         q = self.qs[l] if q is None else q
+        out = self.out[l] if out is None else out
         bd.quantize_query(self.ctx, l, q, self.qp[l], stream)
         if ev is not None:
             ev[0].record()
@@ -164,7 +191,7 @@ class DecodeWorkload:
         tk, tv = self.tails[l]
         gk, gv = self.gscales[l]
         bd.decode_attention(self.ctx, l, self.qp[l], q, self.pools[l], self.block_table, self.seq_lens, sk, sv,
-                            tk, tv, self.tau, gk, gv, self.out[l], self.ws, stream)
+                            tk, tv, self.tau, gk, gv, out, self.ws, stream)
         if ev is not None:
             ev[1].record()
 
@@ -188,19 +215,23 @@ def graphed(fn, torch):
     return g.replay
 
 
-def timed(fn, steps, warmup, stream, torch, dist=None):
+def timed(fn, steps, warmup, stream, torch, dist=None, clocks=None):
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    if clocks is not None:
+        clocks.mark_begin()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0.record(stream)
     for _ in range(steps):
         fn()
-    t1.record()
+    t1.record(stream)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark_end()
     if dist is not None:
         dist.barrier()
     return t0.elapsed_time(t1) / steps
@@ -316,13 +347,13 @@ def main():
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
     clocks = ClockSampler(local)
     clocks.start()
-    ms = timed(fn, args.steps, args.warmup, stream, torch, pg)
+    ms = timed(fn, args.steps, args.warmup, stream, torch, pg, clocks)
+    clk = clocks.stop()
     durs = []
-    for _ in range(max(3, args.steps // 2)):
+    for _ in range(10):
         wl.step(evs=evs)
         torch.cuda.synchronize()
         durs += [a.elapsed_time(b) for a, b in evs]
-    clk = clocks.stop()
     err = bd.read_device_error(wl.ctx)
     if err != bd.OK:
         raise RuntimeError(f"device error word: {bd.status_string(err)}")
@@ -335,24 +366,27 @@ def main():
     step_bytes = wl.bytes_per_layer * args.layers
     achieved = wl.bytes_per_layer / (dec_ms * 1e-3) / 1e9
 
-    # ---------------- end to end through the C ABI with host buffers
-    q_host = [q.cpu().pin_memory() for q in wl.qs]
-    out_host = [torch.empty(1, HQ, D, dtype=torch.float32).pin_memory() for _ in range(args.layers)]
-    q_dev = [torch.empty_like(q) for q in wl.qs]
+    # ---------------- end to end through the C ABI with host buffers: one
+    # host->device copy of the step's queries (all layers) from pinned memory,
+    # the layers, one device->host copy of the step's outputs
+    q_host = torch.stack([q for q in wl.qs]).cpu().pin_memory()          # [layers][1][Hq][D] bf16
+    out_host = torch.empty(args.layers, 1, HQ, D, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(q_host, device=device)
+    out_dev = torch.empty(args.layers, 1, HQ, D, dtype=torch.float32, device=device)
 
     def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
         for l in range(args.layers):
-            q_dev[l].copy_(q_host[l], non_blocking=True)
-            wl.layer(l, q=q_dev[l])
-            out_host[l].copy_(wl.out[l], non_blocking=True)
+            wl.layer(l, q=q_dev[l], out=out_dev[l])
+        out_host.copy_(out_dev, non_blocking=True)
 
     e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg)
     if pg is not None:
         t = torch.tensor([e2e_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t)
-    h2d = sum(q.numel() * q.element_size() for q in q_host)
-    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
 
     tau_sweep = None
     if args.tau_sweep:
@@ -377,14 +411,14 @@ def main():
         "config": {"workload": f"decode {args.ctx}-token ctx, batch 1, {args.layers} layers, 32q/8kv heads, d128, "
                                f"NVFP4 full recipe, tau {args.tau}, shuffled 128-token pages",
                    "global_batch": world, "seq_len": args.ctx, "layers": args.layers,
-                   "l2": "not flushed: each step streams 36 distinct layers' pools "
+                   "l2": f"not flushed: each step streams {args.layers} distinct layers' pools "
                          f"({step_bytes / 1e9:.2f} GB) >> 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "packed_kv_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "packed_kv_frac_of_peak": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+ split combine)", "achieved": achieved,
                      "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": None, "bytes_per_launch": wl_bytes_note(args)},
+                     "traffic": decode_traffic(args), "bytes_per_launch": wl_bytes_note(args)},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "µs/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * args.layers * 2,
@@ -406,6 +440,30 @@ def main():
     if pg is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# DRAM bytes (read + write) of one decode_kernel launch on the 131072-token
+# context, from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on a 2-layer
+# run of this bench; a launch's traffic does not depend on the layer count.
+# Valid only for the kernel sources it was taken on: reported as null once
+# their hash differs.
+DECODE_TRAFFIC = {"sources_sha256_16": "565b021d51fc70ec", "ctx": 131072, "bytes": 151497472 + 2944000}
+DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h")
+
+
+def decode_sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "nvfp4_kv_cache_bd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def decode_traffic(args):
+    if decode_sources_hash() != DECODE_TRAFFIC["sources_sha256_16"] or args.ctx != DECODE_TRAFFIC["ctx"]:
+        return None
+    return DECODE_TRAFFIC["bytes"]
 
 
 def wl_bytes_note(args):
