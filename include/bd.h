@@ -129,7 +129,10 @@ const char* bd_status_string(int status);
 
 /* Copy one layer's static key mean mu [num_kv_heads][128] fp32 from HOST
  * memory into the context ([cfg] RECIPE key_smoothing; KEY_SHIFT_SIDECAR holds
- * these means).  The default mean of every layer is zero.  Synchronous. */
+ * these means).  The default mean of every layer is zero.  Synchronous: it
+ * returns once the copy has landed in device memory, so every later launch
+ * reads the new mean.  Do not call it while a launch that reads this layer's
+ * mean may still be running. */
 int bd_set_key_shift(bd_ctx* ctx, int layer, const float* mu_host);
 
 /* Bytes of one pool record (9216 NVFP4, 8704 MXFP4); a layer's pool holds

@@ -106,7 +106,11 @@ int bd_set_key_shift(bd_ctx* ctx, int layer, const float* mu_host) {
         if (!isfinite(mu_host[i])) return BD_ERR_INVALID_ARG;
     int st = ensure_device(ctx);
     if (st != BD_OK) return st;
-    return cuda_status(cudaMemcpy((void*)layer_mu(ctx, layer), mu_host, n * sizeof(float), cudaMemcpyHostToDevice));
+    // A copy from pageable memory may return before its DMA lands; wait for
+    // it so that every kernel launched afterwards reads the new mean.
+    cudaError_t e = cudaMemcpyAsync((void*)layer_mu(ctx, layer), mu_host, n * sizeof(float), cudaMemcpyHostToDevice, 0);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+    return cuda_status(e);
 }
 
 size_t bd_record_bytes(const bd_ctx* ctx) { return ctx ? (size_t)bd::record_bytes(ctx->cfg.format) : 0; }

@@ -14,7 +14,7 @@
 // sequence's FP4 pages.
 //
 // FP4 split CTA: warp 4 is the producer; one elected lane streams each
-// page's K and V records (9216 B each in NVFP4) into a 6-stage shared-memory
+// page's K and V records (9216 B each in NVFP4) into a 5-stage shared-memory
 // ring with cp.async.bulk (TMA), completing on per-stage "full" mbarriers.
 // Warps 0..3 consume whole pages round-robin (page k -> warp k % 4), so a
 // page's softmax maximum never crosses warps and each warp carries eight
@@ -63,6 +63,8 @@ constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(
 struct Ctl {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
+    unsigned long long cbar;   // the split combine's staging copy
+    int cpad[2];
     float wm[kConsumers][4];   // per-warp running max per head (log2 units)
     float wl[kConsumers][4];   // per-warp softmax denominator per head
     int abort_flag;
@@ -71,12 +73,14 @@ struct Ctl {
     int consumed[kConsumers];  // first page index each warp did not consume
     int is_last;
 };
-constexpr int kScratchBytes = kConsumers * 8 * 2 * 32 * 4;   // per-warp score scratch
-constexpr int kPTabBytes = 3 * 128 * 4;                        // scale tables (see decode_kernel)
+constexpr int kScratchBytes = 2 * 4 * kMaxSplits * 4;          // the split combine's weights
+constexpr int kPTabBytes = 2 * 128 * 4;                        // scale tables (see decode_kernel)
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes + kPTabBytes;
 static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
-static_assert(sizeof(Ctl) % 16 == 0, "score scratch must stay 16-byte aligned");
+static_assert(sizeof(Ctl) % 16 == 0, "the scratch after Ctl must stay 16-byte aligned");
 static_assert(4 * kMaxSplits * kPartStride * 4 <= kRingBytes, "the combine stages a head group's partials in the ring");
+static_assert(2 * 4 * kMaxSplits * 4 <= kScratchBytes, "the combine's weights fit the scratch");
+static_assert(kMaxSplits <= 64, "the combine handles two splits per lane");
 
 __device__ __forceinline__ float ex2(float x) {
     float r;
@@ -268,8 +272,6 @@ template <int FMT, int PM>
 __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t* smem, Ctl* ctl, int warp,
                               int lane) {
     const int g = lane >> 2, t = lane & 3;
-    // this warp's score scratch: [8 blocks][2 tokens][32 lanes] fp32
-    float* sS = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl)) + warp * (8 * 2 * 32);
     griddep_wait();
     const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
     const int hq = a.hq;
@@ -322,10 +324,9 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     const float ccf = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
     const float tau = a.tau;
     // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c)
-    // f16x2, [256,384) (sd, sd) f16x2
+    // f16x2
     const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
     const uint32_t* ptab_sdc = reinterpret_cast<const uint32_t*>(ptab_rcp + 128);
-    const uint32_t* ptab_sbc = reinterpret_cast<const uint32_t*>(ptab_rcp + 256);
     const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
     const int gs = g & 3;
 
@@ -350,27 +351,28 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         const uint8_t* Ks = smem + s * kStageBytes;
         const uint8_t* Vs = Ks + kMaxRec;
 
-        // ---------------- QK, four 16-token blocks per iteration: log2-scaled
-        // scores of head t for tokens 16mi+g and 16mi+g+8 go to the scratch
+        // ---------------- QK over the eight 16-token blocks: log2-scaled
+        // scores of head t for tokens 16mi+g and 16mi+g+8 stay in registers
+        float sc[16];
         float mp = -INFINITY;
-#pragma unroll 1
-        for (int m2 = 0; m2 < 8; m2 += 4) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int mi = m2 + u;
+        for (int mi = 0; mi < 8; ++mi) {
+            {
                 const int tok0 = 16 * mi + g, tok1 = tok0 + 8;
                 const uint4 c0 = lds128(Ks + tok0 * 64 + 16 * t);
                 const uint4 c1 = lds128(Ks + tok1 * 64 + 16 * t);
                 uint32_t s0lo, s0hi, s1lo, s1hi;
                 float fk0 = 1.0f, fk1 = 1.0f;
                 if (FMT == BD_FORMAT_NVFP4) {
-                    // (sd, sd) f16x2 of blocks 2t, 2t+1 of both rows from the table
-                    const uint8_t* sc0 = Ks + kCodeBytes + tok0 * 8 + 2 * t;
-                    const uint8_t* sc1 = Ks + kCodeBytes + tok1 * 8 + 2 * t;
-                    s0lo = ptab_sbc[sc0[0]];
-                    s0hi = ptab_sbc[sc0[1]];
-                    s1lo = ptab_sbc[sc1[0]];
-                    s1hi = ptab_sbc[sc1[1]];
+                    // scale bytes of blocks 2t, 2t+1 of both rows, one 16-bit
+                    // load per row, widened exactly to f16 and broadcast to
+                    // (sd, sd) pairs
+                    const uint32_t h0 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok0 * 8 + 2 * t));
+                    const uint32_t h1 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok1 * 8 + 2 * t));
+                    s0lo = bcast_lo(h0);
+                    s0hi = bcast_hi(h0);
+                    s1lo = bcast_lo(h1);
+                    s1hi = bcast_hi(h1);
                 } else {
                     const int e0 = Ks[kCodeBytes + tok0 * 4 + t], e1 = Ks[kCodeBytes + tok1 * 4 + t];
                     int m0 = max(e0, __shfl_xor_sync(kFull, e0, 1));
@@ -408,8 +410,8 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                 for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
                 const float s0 = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
                 const float s1 = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
-                sS[(2 * mi) * 32 + lane] = s0;
-                sS[(2 * mi + 1) * 32 + lane] = s1;
+                sc[2 * mi] = s0;
+                sc[2 * mi + 1] = s1;
                 mp = fmaxf(mp, fmaxf(s0, s1));
             }
         }
@@ -467,12 +469,10 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
             for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
         }
         float lpage = 0.0f;
-#pragma unroll 1
-        for (int i2 = 0; i2 < 8; i2 += 4) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i2 + u;
-                const float p0 = ex2(sS[(2 * i) * 32 + lane] - mp), p1 = ex2(sS[(2 * i + 1) * 32 + lane] - mp);
+        for (int i = 0; i < 8; ++i) {
+            {
+                const float p0 = ex2(sc[2 * i] - mp), p1 = ex2(sc[2 * i + 1] - mp);
                 lpage += p0 + p1;
                 uint32_t pv;
                 if (PM == BD_P_NONE) {
@@ -610,43 +610,94 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
 }
 
 // Merge every split of (b, kv head h) into out (run by the last CTA).  The
-// head group's partials are first staged into shared memory with one burst
-// of asynchronous 16-byte copies (a single memory round trip), then each of
-// 128 threads merges 4 consecutive dims of one head.
+// head group's partials, one contiguous block, are first staged into shared
+// memory by a single bulk (TMA) copy.  Warp hh then finds head hh's
+// maximum M over the splits (one warp-wide integer max of order-preserving
+// keys) and the weights w_s = 2^(m_s - M) and w_s l_s (0 for an empty
+// split), one split per lane; finally each of 128 threads sums 4
+// consecutive dims of one head, and the denominator, over the splits.
 __device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem) {
     const int nsplit1 = a.nsplit + 1;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
     float* sp = reinterpret_cast<float*>(smem);                 // [4][nsplit1][132] staged partials
-    const int nvec = 4 * nsplit1 * (kPartStride / 4);           // 16-byte pieces
-    for (int i = tid; i < nvec; i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    float* sw = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl));   // [4][kMaxSplits] weights
+    float* swl = sw + 4 * kMaxSplits;                           // [4][kMaxSplits] weights x l
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
+    const uint32_t bytes = 4u * nsplit1 * kPartStride * 4u;    // a multiple of 16 (528-byte rows)
+    const uint32_t cbar = smem_u32(&ctl->cbar);
+    if (tid == 0) {
+        mbar_init(cbar, 1);
+        fence_mbar_init();
+        // the other splits' partials were written through the generic proxy
+        // (made visible by the ticket's acquire) and the ring was last used
+        // through it too; order both before the async-proxy copy
+        asm volatile("fence.proxy.async;" ::: "memory");
+        mbar_arrive_expect_tx(cbar, bytes);
+        bulk_g2s(smem_u32(sp), base, bytes, cbar);
+    }
+    __syncthreads();   // the barrier is initialised before anyone waits on it
+    const bool landed = mbar_wait_bounded(cbar, 0, kWaitLimitNs, nullptr);
+    if (!__syncthreads_and(landed)) {   // uniform: every thread leaves or none
+        if (tid == 0) record_error(a.err, BD_ERR_TIMEOUT);
+        if (!landed) (void)mbar_wait_bounded(cbar, 0, kWaitLimitNs, nullptr);   // let the copy land first
+        return;
+    }
+    if (warp < 4) {
+        const float* ph = sp + (size_t)warp * nsplit1 * kPartStride;
+        float m[2], l[2];
+        uint32_t key = 0;   // order-preserving u32 key of the largest m with l > 0
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int sidx = lane + 32 * r;
+            m[r] = (sidx < nsplit1) ? ph[sidx * kPartStride] : -INFINITY;
+            l[r] = (sidx < nsplit1) ? ph[sidx * kPartStride + 1] : 0.0f;
+            if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
+        }
+        key = __reduce_max_sync(0xFFFFFFFFu, key);
+        const float M = (key == 0) ? -INFINITY : f32_from_order_key(key);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int sidx = lane + 32 * r;
+            const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
+            if (sidx < nsplit1) {
+                sw[warp * kMaxSplits + sidx] = w;
+                swl[warp * kMaxSplits + sidx] = w * l[r];
+            }
+        }
+    }
     __syncthreads();
     if (tid < kD) {
         const int hh = tid >> 5, d0 = (tid & 31) * 4;
-        const float* ph = sp + (size_t)hh * nsplit1 * kPartStride;
-        float M = -INFINITY;
-        for (int s = 0; s < nsplit1; ++s)
-            if (ph[s * kPartStride + 1] > 0.0f) M = fmaxf(M, ph[s * kPartStride]);
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.0f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < nsplit1; ++s) {
-                const float* p = ph + s * kPartStride;
-                if (!(p[1] > 0.0f)) continue;
-                const float w = ex2(p[0] - M);
-                const float4 v = *reinterpret_cast<const float4*>(p + 4 + d0);
-                num.x = fmaf(w, v.x, num.x);
-                num.y = fmaf(w, v.y, num.y);
-                num.z = fmaf(w, v.z, num.z);
-                num.w = fmaf(w, v.w, num.w);
-                den = fmaf(w, p[1], den);
-            }
+        const float* ph = sp + (size_t)hh * nsplit1 * kPartStride + 4 + d0;
+        const float* wh = sw + hh * kMaxSplits;
+        const float* wlh = swl + hh * kMaxSplits;
+        float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+        float den0 = 0.0f, den1 = 0.0f;
+        int sidx = 0;
+#pragma unroll 4
+        for (; sidx + 1 < nsplit1; sidx += 2) {
+            const float w0 = wh[sidx], w1 = wh[sidx + 1];
+            const float4 v0 = *reinterpret_cast<const float4*>(ph + sidx * kPartStride);
+            const float4 v1 = *reinterpret_cast<const float4*>(ph + (sidx + 1) * kPartStride);
+            n0.x = fmaf(w0, v0.x, n0.x); n0.y = fmaf(w0, v0.y, n0.y);
+            n0.z = fmaf(w0, v0.z, n0.z); n0.w = fmaf(w0, v0.w, n0.w);
+            n1.x = fmaf(w1, v1.x, n1.x); n1.y = fmaf(w1, v1.y, n1.y);
+            n1.z = fmaf(w1, v1.z, n1.z); n1.w = fmaf(w1, v1.w, n1.w);
+            den0 += wlh[sidx];
+            den1 += wlh[sidx + 1];
         }
+        if (sidx < nsplit1) {
+            const float w0 = wh[sidx];
+            const float4 v0 = *reinterpret_cast<const float4*>(ph + sidx * kPartStride);
+            n0.x = fmaf(w0, v0.x, n0.x); n0.y = fmaf(w0, v0.y, n0.y);
+            n0.z = fmaf(w0, v0.z, n0.z); n0.w = fmaf(w0, v0.w, n0.w);
+            den0 += wlh[sidx];
+        }
+        const float den = den0 + den1;
         const float r = (den > 0.0f) ? 1.0f / den : 0.0f;
         *reinterpret_cast<float4*>(a.out + ((size_t)b * a.hq + 4 * h + hh) * kD + d0) =
-            make_float4(num.x * r, num.y * r, num.z * r, num.w * r);
+            make_float4((n0.x + n1.x) * r, (n0.y + n1.y) * r, (n0.z + n1.z) * r, (n0.w + n1.w) * r);
     }
 }
 
@@ -694,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
         if (threadIdx.x < 128) {
             // exact per-byte tables for the E4M3 scale byte bb: the correctly
-            // rounded 1/sd and (sd/c, sd/c) for the probability quantizer, and
-            // (sd, sd) for widening key blocks; all f16x2 entries are exact
+            // rounded 1/sd and the f16x2 pair (sd/c, sd/c) for the probability
+            // quantizer (exact: c is a power of two)
             float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
             const uint32_t bb = threadIdx.x;
             const float sd = e4m3_value(bb);
@@ -704,13 +755,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             const uint32_t sdh = e4m3x2_to_f16x2(bb);
             const uint32_t icc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / cc)));
             reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
-            reinterpret_cast<uint32_t*>(tab)[256 + bb] = bcast_lo(sdh);
         }
         __syncthreads();
         if (warp == kConsumers) {
             // ---------------------------------------------------- producer --
             if (lane == 0) {
                 const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
+                // each page is read once per call: evict it from L2 first
+                const uint64_t policy = l2_evict_first_policy();
                 int k = 0;
                 for (; k < n; ++k) {
                     const int s = k % kStages;
@@ -729,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                     // phase only together with their own page index
                     st_release_shared(&ctl->stage_page[s], k);
                     mbar_arrive_expect_tx(full, 2 * RB);
-                    bulk_g2s(dst, krec, RB, full);
-                    bulk_g2s(dst + kMaxRec, krec + RB, RB, full);
+                    bulk_g2s_hint(dst, krec, RB, full, policy);
+                    bulk_g2s_hint(dst + kMaxRec, krec + RB, RB, full, policy);
                 }
                 ctl->issued = k;
             }
@@ -750,16 +802,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     }
 
     // ---------------- ticket: the last CTA of (b, h) merges all splits
+    // The CTA barrier orders every thread's partial writes before thread 0's
+    // release; the acquire half makes the other splits' partials visible to
+    // the last CTA, whose threads read them (through L2) after the barrier.
     griddep_wait();
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const int ticket = atomicAdd(&a.counters[b * a.hkv + h], 1);
+        int ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(&a.counters[b * a.hkv + h])
+                     : "memory");
         ctl->is_last = (ticket == nsplit1 - 1);
     }
     __syncthreads();
     if (ctl->is_last) {
-        __threadfence();
         combine_splits(a, b, h, smem);
         if (threadIdx.x == 0) a.counters[b * a.hkv + h] = 0;
     }

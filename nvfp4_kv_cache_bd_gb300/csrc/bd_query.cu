@@ -19,9 +19,10 @@ namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// CTA-wide maximum of non-negative values: their IEEE bit patterns order
+// like the values, so one integer warp reduction replaces a shuffle chain.
 __device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
+    v = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(v)));
     const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     __syncthreads();
     if ((threadIdx.x & 31) == 0) red[warp] = v;
@@ -105,16 +106,24 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float* x, f
 
 __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
     __shared__ float red[16];
+    const int b = blockIdx.x;
+    const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
+    const int hq = a.hq;
+    uint8_t* qp = a.qp + (size_t)b * a.stride;
+    // The layer's key mean is context state written only by the synchronous
+    // bd_set_key_shift, never by a kernel: it is read before the wait below.
+    float4 mu4[4] = {};
+    if (a.centering && a.mu) {
+        const float4* mu = reinterpret_cast<const float4*>(a.mu + (j / kGroup) * kD + 16 * c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mu4[i] = mu[i];
+    }
     // Programmatic dependent launch: let the dependent decode launch at once
     // (it streams the layer's static FP4 pages and waits for this grid before
     // it reads the packed query), then wait for the grid that precedes us in
     // the stream, whose outputs may feed q.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int b = blockIdx.x;
-    const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
-    const int hq = a.hq;
-    uint8_t* qp = a.qp + (size_t)b * a.stride;
 
     float x[16];
     {
@@ -131,7 +140,8 @@ __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
     // q.mu on the unrotated query (fp32, lane-partial then a 3-step butterfly)
     float qmu = 0.0f;
     if (a.centering && a.mu) {
-        const float* mu = a.mu + (j / kGroup) * kD + 16 * c;
+        const float mu[16] = {mu4[0].x, mu4[0].y, mu4[0].z, mu4[0].w, mu4[1].x, mu4[1].y, mu4[1].z, mu4[1].w,
+                              mu4[2].x, mu4[2].y, mu4[2].z, mu4[2].w, mu4[3].x, mu4[3].y, mu4[3].z, mu4[3].w};
 #pragma unroll
         for (int i = 0; i < 16; ++i) qmu = fmaf(x[i], mu[i], qmu);
     }
