@@ -14,7 +14,7 @@
 // sequence's FP4 pages.
 //
 // FP4 split CTA: warp 4 is the producer; one elected lane streams each
-// page's K and V records (9216 B each in NVFP4) into a 5-stage shared-memory
+// page's K and V records (9216 B each in NVFP4) into a 6-stage shared-memory
 // ring with cp.async.bulk (TMA), completing on per-stage "full" mbarriers.
 // Warps 0..3 consume whole pages round-robin (page k -> warp k % 4), so a
 // page's softmax maximum never crosses warps and each warp carries eight
@@ -51,7 +51,7 @@ namespace bd {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kConsumers = 4;
 constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kMaxRec = 9216;
@@ -60,7 +60,7 @@ constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages 4 x 43 partials
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
-struct Ctl {
+struct alignas(16) Ctl {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
     unsigned long long cbar;   // the split combine's staging copy
@@ -339,7 +339,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     int k = warp;
     for (; k < n; k += kConsumers) {
         const int s = k % kStages;
-        // Warps take pages round-robin from a 5-stage ring, so a warp may start
+        // Warps take pages round-robin from a 6-stage ring, so a warp may start
         // waiting for fill j of a stage before fill j-1 has landed; the phase
         // parity alone cannot tell fill j-2 from fill j, the page tag can.
         if (!wait_stage_page(smem_u32(&ctl->full[s]), (k / kStages) & 1, &ctl->stage_page[s], k,

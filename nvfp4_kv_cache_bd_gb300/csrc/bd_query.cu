@@ -161,11 +161,13 @@ __global__ void __launch_bounds__(512) query_kernel(const QueryArgs a) {
                 }
 #pragma unroll
         for (int m = 1; m <= 4; m <<= 1) {
-            const bool upper = (c & m) != 0;
+            // p - x in the upper lane, x + p in the lower one: fma(x, +-1, p)
+            // rounds the exact p +- x once, like the add or subtract
+            const float sgn = (c & m) ? -1.0f : 1.0f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float p = __shfl_xor_sync(kFull, x[i], m);
-                x[i] = upper ? __fsub_rn(p, x[i]) : __fadd_rn(x[i], p);
+                const float p = __shfl_xor_sync(kFull, x[i], m);
+                x[i] = __fmaf_rn(x[i], sgn, p);
             }
         }
 #pragma unroll

@@ -17,8 +17,10 @@
 //    chunk c = lane/8), so both nibbles of a V code byte are produced in the
 //    same lane and the 16-token tile is written with 16-byte stores.
 // Every rounding step is the IEEE binary32 operation the oracle performs
-// (explicit __f*_rn intrinsics, so nothing is contracted into an FMA); the
-// E2M1 / E4M3 encodings come from the sm_100-family cvt instructions.
+// (explicit __f*_rn intrinsics, so nothing is contracted into an FMA; the
+// one FMA, in the cross-lane butterflies, multiplies by +-1 and rounds once
+// like the add it replaces); the E2M1 / E4M3 encodings come from the
+// sm_100-family cvt instructions.
 #include "bd_device.cuh"
 
 namespace bd {
@@ -160,11 +162,13 @@ __device__ void write_k_tile(const WriterArgs& a, const uint16_t* src, size_t to
             // strides 16, 32, 64 across lanes c^1, c^2, c^4
 #pragma unroll
             for (int m = 1; m <= 4; m <<= 1) {
-                const bool upper = (c & m) != 0;
+                // p - x in the upper lane, x + p in the lower one: fma(x, +-1, p)
+                // rounds the exact p +- x once, like the add or subtract
+                const float sgn = (c & m) ? -1.0f : 1.0f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float p = __shfl_xor_sync(kFull, x[i], m);
-                    x[i] = upper ? __fsub_rn(p, x[i]) : __fadd_rn(x[i], p);
+                    const float p = __shfl_xor_sync(kFull, x[i], m);
+                    x[i] = __fmaf_rn(x[i], sgn, p);
                 }
             }
 #pragma unroll
