@@ -91,9 +91,6 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
@@ -137,19 +134,6 @@ __device__ __forceinline__ bool wait_stage_page(uint32_t bar, uint32_t parity, c
             else if (now - t0 > kWaitLimitNs) return false;
         }
     }
-}
-
-// a / 6 correctly rounded.  For a >= 2^-100, Markstein's method for division
-// by a constant: q0 = a * RN(1/6), the exact remainder r = a - 6 q0 by one
-// FMA, and one more FMA q0 + r * RN(1/6) (valid while nothing underflows);
-// smaller a takes the IEEE division.  Checked bit for bit against __fdiv_rn
-// for every binary32 a in (0, 8] (the probability block maxima).
-__device__ __forceinline__ float div6(float a) {
-    if (a < 7.888609052210118e-31f) return __fdiv_rn(a, 6.0f);   // 2^-100
-    const float y = 1.0f / 6.0f;
-    const float q0 = __fmul_rn(a, y);
-    const float r = __fmaf_rn(-q0, 6.0f, a);
-    return __fmaf_rn(r, y, q0);
 }
 
 // ------------------------------------------------------ BF16 sink + tail --

@@ -95,6 +95,20 @@ __device__ __forceinline__ float f32_from_order_key(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// a / 6 correctly rounded.  For a >= 2^-100, Markstein's method for division
+// by a constant: q0 = a * RN(1/6), the exact remainder r = a - 6 q0 by one
+// FMA, and one more FMA q0 + r * RN(1/6) (valid while nothing underflows);
+// smaller a takes the IEEE division.  Checked bit for bit against __fdiv_rn
+// for every binary32 a in [0, 8] (the probability block maxima) by
+// tests/div6_check.cu.
+__device__ __forceinline__ float div6(float a) {
+    if (a < 7.888609052210118e-31f) return __fdiv_rn(a, 6.0f);   // 2^-100
+    const float y = 1.0f / 6.0f;
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, 6.0f, a);
+    return __fmaf_rn(r, y, q0);
+}
+
 // ------------------------------------------------------------- f16x2 math --
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -178,6 +192,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared, cached in L2 only.  Both
+// addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
 // L2 policy for data read exactly once: its lines are the first evicted, so

@@ -7,8 +7,10 @@
 // "amax6"), KV_MODES["bitdecoding-mxfp4"] scale_mode "mxfp4_search";
 // freeze-at-fill pages from kv-landlords quant_ab.py (module docstring).
 //
-// Grid: one CTA of 8 warps per (page, kv head, K or V).  Each warp owns one
-// 16-token x 128-dim tile.
+// Grid: one CTA of 8 warps per (page, kv head, K or V).  The CTA first
+// stages the page-head's 128 bf16 rows in shared memory with coalesced
+// 16-byte asynchronous copies; each warp then owns one 16-token x 128-dim
+// tile and reads its lanes' values from there.
 //  K warp: lane = (token r = lane/8 of 4, 16-dim chunk c = lane%8).  The
 //    Hadamard transform runs strides 1..8 inside a lane and strides 16, 32,
 //    64 across lanes c^1, c^2, c^4 by warp shuffles; an NVFP4 block (16 dims)
@@ -27,6 +29,10 @@ namespace bd {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
+// Staged bf16 rows: 256 B plus 16 B, so that both lane layouts read their
+// 16-byte pieces from distinct banks (4 lanes per 4-bank group).
+constexpr int kTilePitch = 272;
+constexpr int kTileBytes = kPage * kTilePitch;
 
 struct Scale {
     uint32_t sb;
@@ -91,12 +97,8 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* x) {
     x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
 }
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+    return *reinterpret_cast<const uint4*>(p);
 }
 
 // MXFP4 candidates e0 = floor(log2 amax) - 2 and e0 + 1, clamped to [-127,127].
@@ -122,28 +124,19 @@ __device__ __forceinline__ void mx_err16(const float* x, int e, float* w) {
 
 // ------------------------------------------------------------------ K tile --
 
-__device__ void write_k_tile(const WriterArgs& a, const uint16_t* src, size_t tok_stride, uint8_t* rec,
-                             int grp, int lane, int h) {
+template <int FMT>
+__device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* rec, int grp, int lane, int h) {
     const int r = lane >> 3, c = lane & 7;
     float mu[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) mu[i] = (a.centering && a.mu) ? a.mu[h * kD + 16 * c + i] : 0.0f;
 
-    uint4 raw[4][2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int tok = 16 * grp + 4 * j + r;
-        const uint16_t* p = src + (size_t)tok * tok_stride + 16 * c;
-        raw[j][0] = ld_stream(p);
-        raw[j][1] = ld_stream(p + 8);
-    }
-
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
         const int tok = 16 * grp + 4 * j + r;
         float x[16];
-        unpack_bf16x8(raw[j][0], x);
-        unpack_bf16x8(raw[j][1], x + 8);
+        unpack_bf16x8(lds128(tile + tok * kTilePitch + 32 * c), x);
+        unpack_bf16x8(lds128(tile + tok * kTilePitch + 32 * c + 16), x + 8);
         if (a.centering) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], mu[i]);
@@ -178,7 +171,7 @@ __device__ void write_k_tile(const WriterArgs& a, const uint16_t* src, size_t to
         uint32_t w0, w1, sb;
         float w[16];
         const float amax = amax_of(x, 16);
-        if (a.format == BD_FORMAT_NVFP4) {
+        if (FMT == BD_FORMAT_NVFP4) {
             Scale s6 = nv_scale(amax, 6.0f, a.gk);
             if (a.key_search) {
                 uint32_t c0, c1;
@@ -213,7 +206,7 @@ __device__ void write_k_tile(const WriterArgs& a, const uint16_t* src, size_t to
             sb = (amax32 == 0.0f) ? 0u : (uint32_t)(e + 127);
         }
         *reinterpret_cast<uint2*>(rec + tok * 64 + 8 * c) = make_uint2(w0, w1);
-        if (a.format == BD_FORMAT_NVFP4) rec[kCodeBytes + tok * 8 + c] = (uint8_t)sb;
+        if (FMT == BD_FORMAT_NVFP4) rec[kCodeBytes + tok * 8 + c] = (uint8_t)sb;
         else if (!(c & 1)) rec[kCodeBytes + tok * 4 + (c >> 1)] = (uint8_t)sb;
     }
 }
@@ -256,39 +249,37 @@ __device__ __forceinline__ int mx_search32(const float* x) {
     return (sbb < sa) ? eb : ea;
 }
 
-__device__ void write_v_tile(const WriterArgs& a, const uint16_t* src, size_t tok_stride, uint8_t* rec,
-                             int grp, int lane) {
+template <int FMT>
+__device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* rec, int grp, int lane) {
     const int p = lane & 7, c = lane >> 3;
     const int t0 = 16 * grp + p, t1 = t0 + 8;
-    float x0[32], x1[32];
-    {
-        const uint16_t* p0 = src + (size_t)t0 * tok_stride + 32 * c;
-        const uint16_t* p1 = src + (size_t)t1 * tok_stride + 32 * c;
-        uint4 u[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            u[k] = ld_stream(p0 + 8 * k);
-            u[4 + k] = ld_stream(p1 + 8 * k);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            unpack_bf16x8(u[k], x0 + 8 * k);
-            unpack_bf16x8(u[4 + k], x1 + 8 * k);
-        }
-    }
+    const uint8_t* r0 = tile + t0 * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
+    const uint8_t* r1 = tile + t1 * kTilePitch + 64 * c;
     uint8_t* codes = rec + (grp * 8 + p) * kD + 32 * c;
     uint32_t words[8];
-    if (a.format == BD_FORMAT_NVFP4) {
+    if (FMT == BD_FORMAT_NVFP4) {
+        // one 16-dim block of both tokens at a time
         uint32_t sbs = 0;
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-            Scale s0 = nv_scale(amax_of(x0 + 16 * blk, 16), 6.0f, a.gv);
-            Scale s1 = nv_scale(amax_of(x1 + 16 * blk, 16), 6.0f, a.gv);
-            enc_pair16(x0 + 16 * blk, x1 + 16 * blk, s0.inv, s0.zero, s1.inv, s1.zero, words + 4 * blk);
+            float x0[16], x1[16];
+            unpack_bf16x8(lds128(r0 + 32 * blk), x0);
+            unpack_bf16x8(lds128(r0 + 32 * blk + 16), x0 + 8);
+            unpack_bf16x8(lds128(r1 + 32 * blk), x1);
+            unpack_bf16x8(lds128(r1 + 32 * blk + 16), x1 + 8);
+            Scale s0 = nv_scale(amax_of(x0, 16), 6.0f, a.gv);
+            Scale s1 = nv_scale(amax_of(x1, 16), 6.0f, a.gv);
+            enc_pair16(x0, x1, s0.inv, s0.zero, s1.inv, s1.zero, words + 4 * blk);
             sbs |= (s0.sb | (s1.sb << 8)) << (16 * blk);
         }
         *reinterpret_cast<uint32_t*>(rec + kCodeBytes + ((grp * 8 + p) * 8 + 2 * c) * 2) = sbs;
     } else {
+        float x0[32], x1[32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            unpack_bf16x8(lds128(r0 + 16 * k), x0 + 8 * k);
+            unpack_bf16x8(lds128(r1 + 16 * k), x1 + 8 * k);
+        }
         const int e0 = mx_search32(x0), e1 = mx_search32(x1);
         const bool z0 = e0 == -128, z1 = e1 == -128;
         const float d0 = z0 ? 0.0f : pow2i(-e0), d1 = z1 ? 0.0f : pow2i(-e1);
@@ -301,7 +292,11 @@ __device__ void write_v_tile(const WriterArgs& a, const uint16_t* src, size_t to
     *reinterpret_cast<uint4*>(codes + 16) = make_uint4(words[4], words[5], words[6], words[7]);
 }
 
-__global__ void __launch_bounds__(256) writer_kernel(const WriterArgs a) {
+// NVFP4 fits three CTAs per SM (85 registers); MXFP4 value blocks keep a
+// whole 32-element block of two tokens in registers.
+template <int FMT>
+__global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 3 : 2) writer_kernel(const WriterArgs a) {
+    extern __shared__ __align__(16) uint8_t tile[];   // [128 tokens][kTilePitch]: this head's bf16 rows
     const int pg = blockIdx.x / a.hkv, h = blockIdx.x % a.hkv;
     const int kv = blockIdx.y;
     const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -309,8 +304,16 @@ __global__ void __launch_bounds__(256) writer_kernel(const WriterArgs a) {
     uint8_t* rec = a.pool + ((page * a.hkv + h) * 2 + kv) * (int64_t)record_bytes(a.format);
     const size_t tok_stride = (size_t)a.hkv * kD;
     const uint16_t* src = (kv == 0 ? a.k : a.v) + ((size_t)pg * kPage * a.hkv + h) * kD;
-    if (kv == 0) write_k_tile(a, src, tok_stride, rec, grp, lane, h);
-    else write_v_tile(a, src, tok_stride, rec, grp, lane);
+    // stage the page-head's 128 rows (256 B each) with coalesced 16-byte copies
+    for (int q = threadIdx.x; q < kPage * 16; q += blockDim.x) {
+        const int row = q >> 4, ch = q & 15;
+        cp_async16(smem_u32(tile + row * kTilePitch + 16 * ch), src + (size_t)row * tok_stride + 8 * ch);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (kv == 0) write_k_tile<FMT>(a, tile, rec, grp, lane, h);
+    else write_v_tile<FMT>(a, tile, rec, grp, lane);
 }
 
 }  // namespace
@@ -318,7 +321,10 @@ __global__ void __launch_bounds__(256) writer_kernel(const WriterArgs a) {
 cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
     dim3 grid((unsigned)(a.n * a.hkv), 2);
-    writer_kernel<<<grid, 256, 0, s>>>(a);
+    if (a.format == BD_FORMAT_NVFP4)
+        writer_kernel<BD_FORMAT_NVFP4><<<grid, 256, kTileBytes, s>>>(a);
+    else
+        writer_kernel<BD_FORMAT_MXFP4><<<grid, 256, kTileBytes, s>>>(a);
     return cudaGetLastError();
 }
 
