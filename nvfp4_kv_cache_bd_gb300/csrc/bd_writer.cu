@@ -33,6 +33,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // 16-byte pieces from distinct banks (4 lanes per 4-bank group).
 constexpr int kTilePitch = 272;
 constexpr int kTileBytes = kPage * kTilePitch;
+constexpr int kSTabBytes = 2 * 128 * 4;   // NVFP4 scale tables after the tile
 
 struct Scale {
     uint32_t sb;
@@ -41,15 +42,39 @@ struct Scale {
 };
 
 // NVFP4 scale of a block: t = m*g, s = amax/t -> E4M3 byte, S = E4M3*g, 1/S.
-__device__ __forceinline__ Scale nv_scale(float amax, float m, float g) {
+// stab holds S and RN(1/S) for every byte (scale_tables); s >= 0, so the
+// byte is below 128.
+__device__ __forceinline__ Scale nv_scale(float amax, float m, float g, const float* stab) {
     Scale r;
     float t = __fmul_rn(m, g);
     float s = __fdiv_rn(amax, t);
     r.sb = e4m3(s);
-    r.S = __fmul_rn(e4m3_value(r.sb), g);
-    r.inv = __frcp_rn(r.S);
+    r.S = stab[r.sb];
+    r.inv = stab[128 + r.sb];
     r.zero = (r.S == 0.0f) || isinf(r.inv);
     return r;
+}
+
+// Per-CTA tables for the CTA's per-tensor scale g: S_b = E4M3(b) * g and its
+// correctly rounded reciprocal, for the 128 non-negative scale bytes b.
+__device__ __forceinline__ void scale_tables(float g, float* stab) {
+    if (threadIdx.x < 128) {
+        const float S = __fmul_rn(e4m3_value(threadIdx.x), g);
+        stab[threadIdx.x] = S;
+        stab[128 + threadIdx.x] = __frcp_rn(S);
+    }
+}
+
+// Two values -> one byte of E2M1 codes (lo in bits 3..0), and that byte
+// decoded back to f16x2 (exact), from one conversion register.
+__device__ __forceinline__ uint32_t e2m1x2_enc_dec(float lo, float hi, uint32_t& f16x2) {
+    uint32_t byte, h;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\tcvt.rn.f16x2.e2m1x2 %1, t;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(byte), "=r"(h)
+        : "f"(hi), "f"(lo));
+    f16x2 = h;
+    return byte;
 }
 
 // Squared-error tree over 16 terms: w[i] += w[i+8], then +4, +2, +1.
@@ -70,14 +95,15 @@ __device__ __forceinline__ void enc16(const float* x, float S, float inv, bool z
     w1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        uint32_t byte = 0;
-        if (!zero) byte = e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+        uint32_t byte = 0, hv = 0;
+        if (!zero) byte = e2m1x2_enc_dec(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv), hv);
         if (i < 4) w0 |= byte << (8 * i);
         else w1 |= byte << (8 * (i - 4));
         if (kErr) {
-            float2 val = f16x2_to_float2(e2m1x2_to_f16x2(byte));
-            float e0 = __fsub_rn(x[2 * i], zero ? 0.0f : __fmul_rn(val.x, S));
-            float e1 = __fsub_rn(x[2 * i + 1], zero ? 0.0f : __fmul_rn(val.y, S));
+            // a zero block decodes to 0 and S is finite, so x_hat = 0 * S = +0
+            const float2 val = f16x2_to_float2(hv);
+            const float e0 = __fsub_rn(x[2 * i], __fmul_rn(val.x, S));
+            const float e1 = __fsub_rn(x[2 * i + 1], __fmul_rn(val.y, S));
             w[2 * i] = __fmul_rn(e0, e0);
             w[2 * i + 1] = __fmul_rn(e1, e1);
         }
@@ -125,7 +151,8 @@ __device__ __forceinline__ void mx_err16(const float* x, int e, float* w) {
 // ------------------------------------------------------------------ K tile --
 
 template <int FMT>
-__device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* rec, int grp, int lane, int h) {
+__device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, const float* stab, uint8_t* rec, int grp,
+                             int lane, int h) {
     const int r = lane >> 3, c = lane & 7;
     float mu[16];
 #pragma unroll
@@ -172,12 +199,12 @@ __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* 
         float w[16];
         const float amax = amax_of(x, 16);
         if (FMT == BD_FORMAT_NVFP4) {
-            Scale s6 = nv_scale(amax, 6.0f, a.gk);
+            Scale s6 = nv_scale(amax, 6.0f, a.gk, stab);
             if (a.key_search) {
                 uint32_t c0, c1;
                 enc16<true>(x, s6.S, s6.inv, s6.zero, c0, c1, w);
                 const float e6 = tree16(w);
-                Scale s4 = nv_scale(amax, 4.0f, a.gk);
+                Scale s4 = nv_scale(amax, 4.0f, a.gk, stab);
                 enc16<true>(x, s4.S, s4.inv, s4.zero, w0, w1, w);
                 const float e4 = tree16(w);
                 sb = s4.sb;
@@ -250,7 +277,8 @@ __device__ __forceinline__ int mx_search32(const float* x) {
 }
 
 template <int FMT>
-__device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* rec, int grp, int lane) {
+__device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, const float* stab, uint8_t* rec, int grp,
+                             int lane) {
     const int p = lane & 7, c = lane >> 3;
     const int t0 = 16 * grp + p, t1 = t0 + 8;
     const uint8_t* r0 = tile + t0 * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
@@ -267,8 +295,8 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* 
             unpack_bf16x8(lds128(r0 + 32 * blk + 16), x0 + 8);
             unpack_bf16x8(lds128(r1 + 32 * blk), x1);
             unpack_bf16x8(lds128(r1 + 32 * blk + 16), x1 + 8);
-            Scale s0 = nv_scale(amax_of(x0, 16), 6.0f, a.gv);
-            Scale s1 = nv_scale(amax_of(x1, 16), 6.0f, a.gv);
+            Scale s0 = nv_scale(amax_of(x0, 16), 6.0f, a.gv, stab);
+            Scale s1 = nv_scale(amax_of(x1, 16), 6.0f, a.gv, stab);
             enc_pair16(x0, x1, s0.inv, s0.zero, s1.inv, s1.zero, words + 4 * blk);
             sbs |= (s0.sb | (s1.sb << 8)) << (16 * blk);
         }
@@ -292,10 +320,10 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, uint8_t* 
     *reinterpret_cast<uint4*>(codes + 16) = make_uint4(words[4], words[5], words[6], words[7]);
 }
 
-// NVFP4 fits three CTAs per SM (85 registers); MXFP4 value blocks keep a
+// NVFP4 fits four CTAs per SM (64 registers); MXFP4 value blocks keep a
 // whole 32-element block of two tokens in registers.
 template <int FMT>
-__global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 3 : 2) writer_kernel(const WriterArgs a) {
+__global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 4 : 2) writer_kernel(const WriterArgs a) {
     extern __shared__ __align__(16) uint8_t tile[];   // [128 tokens][kTilePitch]: this head's bf16 rows
     const int pg = blockIdx.x / a.hkv, h = blockIdx.x % a.hkv;
     const int kv = blockIdx.y;
@@ -310,10 +338,12 @@ __global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 3 : 2) writer_ke
         cp_async16(smem_u32(tile + row * kTilePitch + 16 * ch), src + (size_t)row * tok_stride + 8 * ch);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+    float* stab = reinterpret_cast<float*>(tile + kTileBytes);
+    if (FMT == BD_FORMAT_NVFP4) scale_tables(kv == 0 ? a.gk : a.gv, stab);   // while the copies fly
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (kv == 0) write_k_tile<FMT>(a, tile, rec, grp, lane, h);
-    else write_v_tile<FMT>(a, tile, rec, grp, lane);
+    if (kv == 0) write_k_tile<FMT>(a, tile, stab, rec, grp, lane, h);
+    else write_v_tile<FMT>(a, tile, stab, rec, grp, lane);
 }
 
 }  // namespace
@@ -322,7 +352,7 @@ cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
     dim3 grid((unsigned)(a.n * a.hkv), 2);
     if (a.format == BD_FORMAT_NVFP4)
-        writer_kernel<BD_FORMAT_NVFP4><<<grid, 256, kTileBytes, s>>>(a);
+        writer_kernel<BD_FORMAT_NVFP4><<<grid, 256, kTileBytes + kSTabBytes, s>>>(a);
     else
         writer_kernel<BD_FORMAT_MXFP4><<<grid, 256, kTileBytes, s>>>(a);
     return cudaGetLastError();
