@@ -7,10 +7,10 @@
 // "amax6"), KV_MODES["bitdecoding-mxfp4"] scale_mode "mxfp4_search";
 // freeze-at-fill pages from kv-landlords quant_ab.py (module docstring).
 //
-// Grid: one CTA of 8 warps per (page, kv head, K or V).  The CTA first
-// stages the page-head's 128 bf16 rows in shared memory with coalesced
-// 16-byte asynchronous copies; each warp then owns one 16-token x 128-dim
-// tile and reads its lanes' values from there.
+// Grid: one CTA of 4 warps per (page, kv head, K or V, half page).  The CTA
+// first stages its 64 bf16 rows in shared memory with coalesced 16-byte
+// asynchronous copies; each warp then owns one 16-token x 128-dim tile and
+// reads its lanes' values from there.
 //  K warp: lane = (token r = lane/8 of 4, 16-dim chunk c = lane%8).  The
 //    Hadamard transform runs strides 1..8 inside a lane and strides 16, 32,
 //    64 across lanes c^1, c^2, c^4 by warp shuffles; an NVFP4 block (16 dims)
@@ -32,7 +32,11 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 // Staged bf16 rows: 256 B plus 16 B, so that both lane layouts read their
 // 16-byte pieces from distinct banks (4 lanes per 4-bank group).
 constexpr int kTilePitch = 272;
-constexpr int kTileBytes = kPage * kTilePitch;
+// A CTA covers half a page (64 tokens, 4 warps of 16): small CTAs spread the
+// heavy key tiles evenly over the SMs.
+constexpr int kCtaRows = 64;
+constexpr int kCtaThreads = 2 * kCtaRows;
+constexpr int kTileBytes = kCtaRows * kTilePitch;
 constexpr int kSTabBytes = 2 * 128 * 4;   // NVFP4 scale tables after the tile
 
 struct Scale {
@@ -151,8 +155,8 @@ __device__ __forceinline__ void mx_err16(const float* x, int e, float* w) {
 // ------------------------------------------------------------------ K tile --
 
 template <int FMT>
-__device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, const float* stab, uint8_t* rec, int grp,
-                             int lane, int h) {
+__device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, int row0, const float* stab, uint8_t* rec,
+                             int grp, int lane, int h) {
     const int r = lane >> 3, c = lane & 7;
     float mu[16];
 #pragma unroll
@@ -162,8 +166,8 @@ __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, const flo
     for (int j = 0; j < 4; ++j) {
         const int tok = 16 * grp + 4 * j + r;
         float x[16];
-        unpack_bf16x8(lds128(tile + tok * kTilePitch + 32 * c), x);
-        unpack_bf16x8(lds128(tile + tok * kTilePitch + 32 * c + 16), x + 8);
+        unpack_bf16x8(lds128(tile + (tok - row0) * kTilePitch + 32 * c), x);
+        unpack_bf16x8(lds128(tile + (tok - row0) * kTilePitch + 32 * c + 16), x + 8);
         if (a.centering) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], mu[i]);
@@ -277,12 +281,12 @@ __device__ __forceinline__ int mx_search32(const float* x) {
 }
 
 template <int FMT>
-__device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, const float* stab, uint8_t* rec, int grp,
-                             int lane) {
+__device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, int row0, const float* stab, uint8_t* rec,
+                             int grp, int lane) {
     const int p = lane & 7, c = lane >> 3;
     const int t0 = 16 * grp + p, t1 = t0 + 8;
-    const uint8_t* r0 = tile + t0 * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
-    const uint8_t* r1 = tile + t1 * kTilePitch + 64 * c;
+    const uint8_t* r0 = tile + (t0 - row0) * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
+    const uint8_t* r1 = tile + (t1 - row0) * kTilePitch + 64 * c;
     uint8_t* codes = rec + (grp * 8 + p) * kD + 32 * c;
     uint32_t words[8];
     if (FMT == BD_FORMAT_NVFP4) {
@@ -320,20 +324,21 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, const flo
     *reinterpret_cast<uint4*>(codes + 16) = make_uint4(words[4], words[5], words[6], words[7]);
 }
 
-// NVFP4 fits four CTAs per SM (64 registers); MXFP4 value blocks keep a
+// NVFP4 fits eight CTAs per SM (64 registers); MXFP4 value blocks keep a
 // whole 32-element block of two tokens in registers.
 template <int FMT>
-__global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 4 : 2) writer_kernel(const WriterArgs a) {
-    extern __shared__ __align__(16) uint8_t tile[];   // [128 tokens][kTilePitch]: this head's bf16 rows
+__global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) writer_kernel(const WriterArgs a) {
+    extern __shared__ __align__(16) uint8_t tile[];   // [kCtaRows tokens][kTilePitch]: this head's bf16 rows
     const int pg = blockIdx.x / a.hkv, h = blockIdx.x % a.hkv;
     const int kv = blockIdx.y;
-    const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = kCtaRows * blockIdx.z;            // first token of this CTA's half page
+    const int grp = (row0 >> 4) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int64_t page = a.dst_pages[pg];
     uint8_t* rec = a.pool + ((page * a.hkv + h) * 2 + kv) * (int64_t)record_bytes(a.format);
     const size_t tok_stride = (size_t)a.hkv * kD;
-    const uint16_t* src = (kv == 0 ? a.k : a.v) + ((size_t)pg * kPage * a.hkv + h) * kD;
-    // stage the page-head's 128 rows (256 B each) with coalesced 16-byte copies
-    for (int q = threadIdx.x; q < kPage * 16; q += blockDim.x) {
+    const uint16_t* src = (kv == 0 ? a.k : a.v) + (((size_t)pg * kPage + row0) * a.hkv + h) * kD;
+    // stage the CTA's rows (256 B each) with coalesced 16-byte copies
+    for (int q = threadIdx.x; q < kCtaRows * 16; q += blockDim.x) {
         const int row = q >> 4, ch = q & 15;
         cp_async16(smem_u32(tile + row * kTilePitch + 16 * ch), src + (size_t)row * tok_stride + 8 * ch);
     }
@@ -342,19 +347,19 @@ __global__ void __launch_bounds__(256, FMT == BD_FORMAT_NVFP4 ? 4 : 2) writer_ke
     if (FMT == BD_FORMAT_NVFP4) scale_tables(kv == 0 ? a.gk : a.gv, stab);   // while the copies fly
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (kv == 0) write_k_tile<FMT>(a, tile, stab, rec, grp, lane, h);
-    else write_v_tile<FMT>(a, tile, stab, rec, grp, lane);
+    if (kv == 0) write_k_tile<FMT>(a, tile, row0, stab, rec, grp, lane, h);
+    else write_v_tile<FMT>(a, tile, row0, stab, rec, grp, lane);
 }
 
 }  // namespace
 
 cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
-    dim3 grid((unsigned)(a.n * a.hkv), 2);
+    dim3 grid((unsigned)(a.n * a.hkv), 2, kPage / kCtaRows);
     if (a.format == BD_FORMAT_NVFP4)
-        writer_kernel<BD_FORMAT_NVFP4><<<grid, 256, kTileBytes + kSTabBytes, s>>>(a);
+        writer_kernel<BD_FORMAT_NVFP4><<<grid, kCtaThreads, kTileBytes + kSTabBytes, s>>>(a);
     else
-        writer_kernel<BD_FORMAT_MXFP4><<<grid, 256, kTileBytes, s>>>(a);
+        writer_kernel<BD_FORMAT_MXFP4><<<grid, kCtaThreads, kTileBytes, s>>>(a);
     return cudaGetLastError();
 }
 
