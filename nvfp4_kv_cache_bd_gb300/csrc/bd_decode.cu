@@ -51,26 +51,23 @@ namespace bd {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kStages = 6;
-constexpr int kConsumers = 4;
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kMaxRec = 9216;
-constexpr int kStageBytes = 2 * kMaxRec;
-constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kConsumers = 6;                    // consumer warps; warps 6 and 7 stream K and V
+constexpr int kThreads = (kConsumers + 2) * 32;
+constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
+constexpr int kNK = 6, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
+constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
 constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages 4 x 43 partials
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 struct alignas(16) Ctl {
-    unsigned long long full[kStages];
-    unsigned long long empty[kStages];
+    unsigned long long fullK[kNK], emptyK[kNK];   // K ring
+    unsigned long long fullV[kNV], emptyV[kNV];   // V ring
     unsigned long long cbar;   // the split combine's staging copy
-    int cpad[2];
     float wm[kConsumers][4];   // per-warp running max per head (log2 units)
     float wl[kConsumers][4];   // per-warp softmax denominator per head
     int abort_flag;
-    int issued;
-    int stage_page[kStages];   // page index the stage's latest fill holds (-1: none)
-    int consumed[kConsumers];  // first page index each warp did not consume
+    int next_page;             // next page index a consumer warp takes
+    int tagK[kNK], tagV[kNV];  // page index each slot's latest fill holds (-1: none)
     int is_last;
 };
 constexpr int kScratchBytes = 2 * 4 * kMaxSplits * 4;          // the split combine's weights
@@ -133,6 +130,38 @@ __device__ __forceinline__ bool wait_stage_page(uint32_t bar, uint32_t parity, c
             if (t0 == 0) t0 = now;
             else if (now - t0 > kWaitLimitNs) return false;
         }
+    }
+}
+
+// Element-wise maximum of v[0..7] over the 8 lanes that share lane & 3 (lane
+// bits 2..4), left in every one of them: a reduce-scatter (4 + 2 + 1
+// shuffles) leaves each lane the full maximum of one element, an all-gather
+// (1 + 2 + 4) returns all eight.  14 shuffles instead of 3 per element.
+__device__ __forceinline__ void max8_across_g(float* v, int lane) {
+    const bool b2 = lane & 16, b1 = lane & 8, b0 = lane & 4;
+    float h4[4];   // elements (b2 ? 4 : 0) + 0..3
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b2 ? v[j] : v[j + 4], keep = b2 ? v[j + 4] : v[j];
+        h4[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, 16));
+    }
+    float h2[2];   // elements (b2 ? 4 : 0) + (b1 ? 2 : 0) + 0..1
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b1 ? h4[j] : h4[j + 2], keep = b1 ? h4[j + 2] : h4[j];
+        h2[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, 8));
+    }
+    // element (b2 ? 4 : 0) + (b1 ? 2 : 0) + (b0 ? 1 : 0), now over all 8 lanes
+    const float h1 = fmaxf(b0 ? h2[1] : h2[0], __shfl_xor_sync(kFull, b0 ? h2[0] : h2[1], 4));
+    const float o1 = __shfl_xor_sync(kFull, h1, 4);
+    const float g2[2] = {b0 ? o1 : h1, b0 ? h1 : o1};
+    const float o2[2] = {__shfl_xor_sync(kFull, g2[0], 8), __shfl_xor_sync(kFull, g2[1], 8)};
+    const float g4[4] = {b1 ? o2[0] : g2[0], b1 ? o2[1] : g2[1], b1 ? g2[0] : o2[0], b1 ? g2[1] : o2[1]};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float o4 = __shfl_xor_sync(kFull, g4[j], 16);
+        v[j] = b2 ? o4 : g4[j];
+        v[j + 4] = b2 ? g4[j] : o4;
     }
 }
 
@@ -320,20 +349,25 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
 #pragma unroll
     for (int bm = 0; bm < 8; ++bm) o[bm][0] = o[bm][1] = o[bm][2] = o[bm][3] = 0.0f;
 
-    int k = warp;
-    for (; k < n; k += kConsumers) {
-        const int s = k % kStages;
-        // Warps take pages round-robin from a 6-stage ring, so a warp may start
-        // waiting for fill j of a stage before fill j-1 has landed; the phase
-        // parity alone cannot tell fill j-2 from fill j, the page tag can.
-        if (!wait_stage_page(smem_u32(&ctl->full[s]), (k / kStages) & 1, &ctl->stage_page[s], k,
-                             &ctl->abort_flag)) {
+    for (;;) {
+        // the next page in order: warps take pages as they become free, so
+        // every warp's pages increase and the lowest unfinished page can
+        // always proceed
+        int k = 0;
+        if (lane == 0) k = atomicAdd(&ctl->next_page, 1);
+        k = __shfl_sync(kFull, k, 0);
+        if (k >= n) break;
+        const int sk = k % kNK, sv = k % kNV;
+        // A warp may start waiting for fill j of a slot before fill j-1 has
+        // landed; the phase parity alone cannot tell fill j-2 from fill j, the
+        // page tag can.
+        if (!wait_stage_page(smem_u32(&ctl->fullK[sk]), (k / kNK) & 1, &ctl->tagK[sk], k, &ctl->abort_flag)) {
             if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
             ctl->abort_flag = 1;
             break;
         }
-        const uint8_t* Ks = smem + s * kStageBytes;
-        const uint8_t* Vs = Ks + kMaxRec;
+        const uint8_t* Ks = smem + sk * kMaxRec;
+        const uint8_t* Vs = smem + (kNK + sv) * kMaxRec;
 
         // ---------------- QK over the eight 16-token blocks: log2-scaled
         // scores of head t for tokens 16mi+g and 16mi+g+8 stay in registers
@@ -400,11 +434,21 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
             }
         }
 
+        // the K slot is free once every lane's key reads are done
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyK[sk]));
+
         // ---------------- page maximum of head t (and of heads 2t, 2t+1)
         mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 4));
         mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 8));
         mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 16));
         const float mpA = __shfl_sync(kFull, mp, srcA), mpB = __shfl_sync(kFull, mp, srcB);
+
+        if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
+            if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+            ctl->abort_flag = 1;
+            break;
+        }
 
         float fv = 1.0f;   // MXFP4: 2^(reference exponent of this lane's V block)
         int ev_ref = 0;
@@ -452,22 +496,33 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
 #pragma unroll
             for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
         }
+        // the page's probabilities first, then the eight blocks' maxima of
+        // u = c P over their 16 tokens with one reduction across the lanes g
+        float pr[16];
         float lpage = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
+            pr[2 * i] = ex2(sc[2 * i] - mp);
+            pr[2 * i + 1] = ex2(sc[2 * i + 1] - mp);
+            lpage += pr[2 * i] + pr[2 * i + 1];
+        }
+        float bmax[8];
+        if (PM != BD_P_NONE) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bmax[i] = fmaxf(pr[2 * i] * ccf, pr[2 * i + 1] * ccf);
+            max8_across_g(bmax, lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             {
-                const float p0 = ex2(sc[2 * i] - mp), p1 = ex2(sc[2 * i + 1] - mp);
-                lpage += p0 + p1;
+                const float p0 = pr[2 * i], p1 = pr[2 * i + 1];
                 uint32_t pv;
                 if (PM == BD_P_NONE) {
                     const __half2 hh = __floats2half2_rn(p0, p1);
                     pv = *reinterpret_cast<const uint32_t*>(&hh);
                 } else {
                     const float u0 = p0 * ccf, u1 = p1 * ccf;
-                    float am = fmaxf(u0, u1);
-                    am = fmaxf(am, __shfl_xor_sync(kFull, am, 4));
-                    am = fmaxf(am, __shfl_xor_sync(kFull, am, 8));
-                    am = fmaxf(am, __shfl_xor_sync(kFull, am, 16));
+                    const float am = bmax[i];
                     const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (am < tau);
                     const float sv = two ? am * 0.5f : div6(am);
                     // scale byte -> 1/sd (correctly rounded) and (sd/c, sd/c) from the tables;
@@ -515,9 +570,9 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                 }
             }
         }
-        // release the stage: every lane's shared-memory reads are done
+        // release the V slot: every lane's shared-memory reads are done
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->empty[s]));
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyV[sv]));
 
         // ---------------- merge the page into the warp's running state
         lacc = fmaf(lacc, ex2(Mt - mnt), wpage * lpage);
@@ -536,13 +591,11 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                 o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
             }
         }
-        __syncwarp();   // the scratch is rewritten by the next page
     }
-    if (lane == 0) ctl->consumed[warp] = k;
 
     // ---------------- hand the warp state to the CTA merge
     __syncthreads();   // (A) all consumers are done with the ring
-    float* sO = reinterpret_cast<float*>(smem);   // [4 warps][4 heads][128]
+    float* sO = reinterpret_cast<float*>(smem);   // [consumer warps][4 heads][128]
     if (t < 2) {
 #pragma unroll
         for (int bm = 0; bm < 8; ++bm) {
@@ -562,7 +615,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     }
 }
 
-// CTA merge of the four warps' states into this split's partial.
+// CTA merge of the consumer warps' states into this split's partial.
 __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint8_t* smem, const Ctl* ctl) {
     const int tid = threadIdx.x;
     if (tid >= 128) return;
@@ -686,7 +739,7 @@ __device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem)
 }
 
 template <int FMT, int PM>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {   // 128 registers
     extern __shared__ __align__(128) uint8_t smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int L = a.seq_lens[b];
@@ -717,16 +770,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         const int n = p1 - p0;
         constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
         if (threadIdx.x == 0) {
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(smem_u32(&ctl->full[s]), 1);
-                mbar_init(smem_u32(&ctl->empty[s]), 1);
+            for (int s = 0; s < kNK; ++s) {
+                mbar_init(smem_u32(&ctl->fullK[s]), 1);
+                mbar_init(smem_u32(&ctl->emptyK[s]), 1);
+                ctl->tagK[s] = -1;
+            }
+            for (int s = 0; s < kNV; ++s) {
+                mbar_init(smem_u32(&ctl->fullV[s]), 1);
+                mbar_init(smem_u32(&ctl->emptyV[s]), 1);
+                ctl->tagV[s] = -1;
             }
             ctl->abort_flag = 0;
-            ctl->issued = 0;
-            for (int st = 0; st < kStages; ++st) ctl->stage_page[st] = -1;
+            ctl->next_page = 0;
             fence_mbar_init();
         }
-        if (threadIdx.x < kConsumers) ctl->consumed[threadIdx.x] = 0;
         if (threadIdx.x < 128) {
             // exact per-byte tables for the E4M3 scale byte bb: the correctly
             // rounded 1/sd and the f16x2 pair (sd/c, sd/c) for the probability
@@ -741,42 +798,46 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
         }
         __syncthreads();
-        if (warp == kConsumers) {
-            // ---------------------------------------------------- producer --
+        if (warp >= kConsumers) {
+            // --------------------------------------------------- producers --
+            // warp 6 streams the pages' K records into the K ring, warp 7 their
+            // V records into the V ring, each in page order
+            const bool isK = (warp == kConsumers);
+            const int N = isK ? kNK : kNV;
+            unsigned long long* fullb = isK ? ctl->fullK : ctl->fullV;
+            unsigned long long* emptyb = isK ? ctl->emptyK : ctl->emptyV;
+            int* tag = isK ? ctl->tagK : ctl->tagV;
+            uint8_t* slots = smem + (isK ? 0 : kNK * kMaxRec);
             if (lane == 0) {
                 const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
                 // each page is read once per call: evict it from L2 first
                 const uint64_t policy = l2_evict_first_policy();
-                int k = 0;
-                for (; k < n; ++k) {
-                    const int s = k % kStages;
-                    if (k >= kStages &&
-                        !mbar_wait_bounded(smem_u32(&ctl->empty[s]), ((k / kStages) - 1) & 1, kWaitLimitNs,
-                                           &ctl->abort_flag)) {
+                for (int k = 0; k < n; ++k) {
+                    const int s = k % N;
+                    if (k >= N && !mbar_wait_bounded(smem_u32(&emptyb[s]), ((k / N) - 1) & 1, kWaitLimitNs,
+                                                     &ctl->abort_flag)) {
                         if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
                         ctl->abort_flag = 1;
                         break;
                     }
                     const int64_t phys = bt[k];
-                    const uint8_t* krec = a.pool + ((phys * a.hkv + h) * 2) * (int64_t)RB;
-                    const uint32_t full = smem_u32(&ctl->full[s]);
-                    const uint32_t dst = smem_u32(smem + s * kStageBytes);
+                    const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
+                    const uint32_t full = smem_u32(&fullb[s]);
                     // tag the fill before it is armed: consumers accept a completed
                     // phase only together with their own page index
-                    st_release_shared(&ctl->stage_page[s], k);
-                    mbar_arrive_expect_tx(full, 2 * RB);
-                    bulk_g2s_hint(dst, krec, RB, full, policy);
-                    bulk_g2s_hint(dst + kMaxRec, krec + RB, RB, full, policy);
+                    st_release_shared(&tag[s], k);
+                    mbar_arrive_expect_tx(full, RB);
+                    bulk_g2s_hint(smem_u32(slots + s * kMaxRec), rec, RB, full, policy);
                 }
-                ctl->issued = k;
             }
             __syncthreads();   // (A)
-            // drain copies an aborted run left in flight before the ring is reused
+            // an aborted run drains the copies it left in flight before the ring
+            // is reused: a slot's last fill is the only one that can be pending
             if (lane == 0 && ctl->abort_flag) {
-                for (int kk = 0; kk < ctl->issued; ++kk)
-                    if (kk >= ctl->consumed[kk % kConsumers])
-                        (void)mbar_wait_bounded(smem_u32(&ctl->full[kk % kStages]), (kk / kStages) & 1,
-                                                kWaitLimitNs, nullptr);
+                for (int s = 0; s < N; ++s) {
+                    const int f = tag[s];
+                    if (f >= 0) (void)mbar_wait_bounded(smem_u32(&fullb[s]), (f / N) & 1, kWaitLimitNs, nullptr);
+                }
             }
         } else {
             consume_pages<FMT, PM>(a, b, h, n, smem, ctl, warp, lane);   // contains (A)
