@@ -444,31 +444,10 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 16));
         const float mpA = __shfl_sync(kFull, mp, srcA), mpB = __shfl_sync(kFull, mp, srcB);
 
-        if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
-            if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
-            ctl->abort_flag = 1;
-            break;
-        }
-
-        float fv = 1.0f;   // MXFP4: 2^(reference exponent of this lane's V block)
-        int ev_ref = 0;
-        if (FMT == BD_FORMAT_MXFP4) {
-            int em = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
-                const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
-                em = max(em, (int)max(max(e0 & 0xFF, e0 >> 8), max(e1 & 0xFF, e1 >> 8)));
-            }
-            em = max(em, __shfl_xor_sync(kFull, em, 1));
-            em = max(em, __shfl_xor_sync(kFull, em, 2));
-            em = max(em, __shfl_xor_sync(kFull, em, 4));
-            ev_ref = em;
-            fv = pow2i(em - 127);
-        }
-
-        // ---------------- per 16-token block: probabilities, their FP4
-        // quantization, and P V.  NVFP4: the running max is updated first and
+        // ---------------- per 16-token block: probabilities and their FP4
+        // quantization into P V's B fragments, all before the page's V record
+        // is awaited (its slot is held only for P V).  NVFP4: the running max
+        // is updated first and
         // the page weight 2^(m_p - M) is folded into the f16 Phat operand, so
         // P V accumulates straight into O (one f16 rounding, < 2^-11
         // relative, per weighted Phat).  MXFP4 keeps a per-page O_p because
@@ -507,6 +486,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
             lpage += pr[2 * i] + pr[2 * i + 1];
         }
         float bmax[8];
+        uint32_t bfr[16];   // B fragments of Phat for P V, two per block
         if (PM != BD_P_NONE) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) bmax[i] = fmaxf(pr[2 * i] * ccf, pr[2 * i + 1] * ccf);
@@ -535,8 +515,38 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                 if (FMT == BD_FORMAT_NVFP4) pv = hmul2(pv, wh);
                 // lanes with g >= 4 feed the padding columns 4..7 (duplicates of
                 // heads 0..3); their outputs are never read
-                const uint32_t b01 = __shfl_sync(kFull, pv, 4 * t + gs);
-                const uint32_t b23 = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
+                bfr[2 * i] = __shfl_sync(kFull, pv, 4 * t + gs);
+                bfr[2 * i + 1] = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
+            }
+        }
+
+        // ---------------- P V: only now is the page's V record needed
+        if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
+            if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+            ctl->abort_flag = 1;
+            break;
+        }
+
+        float fv = 1.0f;   // MXFP4: 2^(reference exponent of this lane's V block)
+        int ev_ref = 0;
+        if (FMT == BD_FORMAT_MXFP4) {
+            int em = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
+                const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
+                em = max(em, (int)max(max(e0 & 0xFF, e0 >> 8), max(e1 & 0xFF, e1 >> 8)));
+            }
+            em = max(em, __shfl_xor_sync(kFull, em, 1));
+            em = max(em, __shfl_xor_sync(kFull, em, 2));
+            em = max(em, __shfl_xor_sync(kFull, em, 4));
+            ev_ref = em;
+            fv = pow2i(em - 127);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            {
+                const uint32_t b01 = bfr[2 * i], b23 = bfr[2 * i + 1];
                 const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * g);
                 const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * g);
                 uint32_t vs0, vs1;
