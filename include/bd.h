@@ -192,7 +192,13 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *                 zero the whole workspace once before its first use; every
  *                 completed call leaves the tickets zero again.  Calls that
  *                 share a workspace must not overlap on the GPU.
- * Query head j reads kv head j / 4; softmax scale 1/sqrt(128). */
+ * Query head j reads kv head j / 4; softmax scale 1/sqrt(128).
+ * Ordering: the kernel may start reading kv_pool and block_table while the
+ * preceding grid in the stream, if it allows programmatic early launch,
+ * still runs (this library's query and decode kernels do); those inputs
+ * must be final before that grid was launched.  q_packed, q, the sink and
+ * tail rows, out and ws are touched only after the preceding grid has
+ * completed. */
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q,
                         const void* kv_pool, const int32_t* block_table, int max_blocks,
                         const int32_t* seq_lens, const void* sink_k, const void* sink_v,
