@@ -188,11 +188,13 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *   k/v_gscale  : the per-tensor scales the layer's pages were written with.
  *   out         : fp32 [B][num_q_heads][128], device.
  *   ws          : device scratch of at least bd_decode_workspace_size(ctx, B,
- *                 max_blocks) bytes.  Its first bytes hold split tickets:
- *                 zero the whole workspace once before its first use; every
- *                 completed call leaves the tickets zero again.  Calls that
- *                 share a workspace must not overlap on the GPU.
+ *                 max_blocks) bytes for the split partials; it needs no
+ *                 initialization.  Calls that share a workspace must not
+ *                 overlap on the GPU.
  * Query head j reads kv head j / 4; softmax scale 1/sqrt(128).
+ * Two kernels are launched on `stream`: the split decode, then the split
+ * combine, which starts under programmatic dependent launch and reads the
+ * partials once the decode grid has completed.
  * Ordering: the kernel may start reading kv_pool and block_table while the
  * preceding grid in the stream, if it allows programmatic early launch,
  * still runs (this library's query and decode kernels do); those inputs
@@ -214,15 +216,16 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
  * front -- and so cannot provide the workspace bd_decode_attention needs.
  * Arguments are those of bd_decode_attention minus ws / ws_bytes; inputs and
  * out are still caller-owned device memory.
- *  - The split tickets and split partials live in one fixed 4 MiB device
- *    array inside the library (every GPU that loads the library holds it
- *    until the process exits).  A call whose tickets and partials need more
+ *  - The split partials live in one fixed 4 MiB device array inside the
+ *    library (every GPU that loads the library holds it until the process
+ *    exits).  A call whose partials need more
  *    (bd_decode_workspace_size(ctx, B, max_blocks) > 4 MiB) is rejected with
  *    BD_ERR_WORKSPACE before anything is launched: use bd_decode_attention
  *    with a workspace instead.
- *  - Every call shares that array and clears its tickets on `stream` first;
- *    calls that overlap on the GPU (other streams, other threads) race and
- *    must be serialized by the caller.
+ *  - Nothing in that array has to start at zero: each call writes every
+ *    partial it reads.  Every call shares the array, so calls that overlap
+ *    on the GPU (other streams, other threads) race and must be serialized
+ *    by the caller.
  *  - The first call on a device looks up the array's device address; make
  *    that first call before capturing a stream into a CUDA graph.
  *  - No cudaMalloc, cudaFree or allocating library routine is called.  A

@@ -167,7 +167,7 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks) {
     if (!ctx || B <= 0 || max_blocks < 0) return 0;
     int ns = 0, pps = 0;
     bd::decode_splits(B, ctx->cfg.num_kv_heads, max_blocks, &ns, &pps);
-    return bd::decode_ws_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ns);
+    return bd::decode_ws_bytes(B, ctx->cfg.num_q_heads, ns);
 }
 
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q, const void* kv_pool,
@@ -200,8 +200,7 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     a.tail_k = static_cast<const uint16_t*>(tail_k);
     a.tail_v = static_cast<const uint16_t*>(tail_v);
     a.out = out;
-    a.counters = static_cast<int*>(ws);
-    a.parts = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + bd::decode_counter_bytes(B, ctx->cfg.num_kv_heads));
+    a.parts = static_cast<float*>(ws);
     a.err = ctx->d_err;
     a.qstride = bd::qpack_stride(ctx->cfg.num_q_heads);
     a.B = B;
@@ -235,15 +234,12 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     const uintptr_t align = (uintptr_t)q_packed | (uintptr_t)kv_pool | (uintptr_t)q | (uintptr_t)sink_k |
                             (uintptr_t)sink_v | (uintptr_t)tail_k | (uintptr_t)tail_v | (uintptr_t)out;
     if (align & 15u) return BD_ERR_INVALID_ARG;
-    // the fixed scratch must hold this call's tickets and split partials
+    // the fixed scratch must hold this call's split partials
     const size_t need = bd_decode_workspace_size(ctx, B, max_blocks);
     if (need > bd::kNoAllocScratchBytes) return BD_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (bd::noalloc_scratch(&scratch) != cudaSuccess) return BD_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t counter_bytes = bd::decode_counter_bytes(B, ctx->cfg.num_kv_heads);
-    // the tickets must start at zero
-    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return BD_ERR_CUDA;
     bd::DecodeArgs a;
     a.qp = static_cast<const uint8_t*>(q_packed);
     a.q = static_cast<const uint16_t*>(q);
@@ -255,8 +251,7 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     a.tail_k = static_cast<const uint16_t*>(tail_k);
     a.tail_v = static_cast<const uint16_t*>(tail_v);
     a.out = out;
-    a.counters = static_cast<int*>(scratch);
-    a.parts = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + counter_bytes);
+    a.parts = static_cast<float*>(scratch);
     // a bounded wait that runs out is recorded only if the context already
     // has its device error word (this path never creates it)
     a.err = ctx->d_err;

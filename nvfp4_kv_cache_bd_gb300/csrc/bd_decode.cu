@@ -33,14 +33,16 @@
 //        stores tokens tau and tau+8 in one byte, which is exactly an
 //        A-fragment register of this MMA; Phat reaches the B-fragment layout
 //        with two warp shuffles.
-//  Each warp merges its pages into a running (M, L, O); at the end the four
-//  warps' states are merged through shared memory into the split partial.
-// The last CTA to finish a (sequence, kv head) -- an atomic ticket in the
-// workspace -- merges all splits: O = sum 2^(m-M) O / sum 2^(m-M) l.
+//  Each warp merges its pages into a running (M, L, O); at the end the
+//  consumer warps' states are merged through shared memory into the split
+//  partial.
+// A second kernel, one CTA per (sequence, query head), merges the splits:
+// O = sum 2^(m-M) O / sum 2^(m-M) l.
 //
-// Launched with programmatic dependent launch: the producer starts streaming
-// pages while the query quantizer still runs; every thread that reads the
-// packed or raw query first waits on the preceding grid.
+// Both are launched with programmatic dependent launch: the producers start
+// streaming pages while the query quantizer still runs; every thread that
+// reads the packed or raw query, or writes the workspace or out, first
+// waits on the preceding grid.
 #include <math.h>
 
 #include <mutex>
@@ -56,27 +58,22 @@ constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
 constexpr int kNK = 6, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
 constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
-constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages 4 x 43 partials
+constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages them in 22.7 KB
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 struct alignas(16) Ctl {
     unsigned long long fullK[kNK], emptyK[kNK];   // K ring
     unsigned long long fullV[kNV], emptyV[kNV];   // V ring
-    unsigned long long cbar;   // the split combine's staging copy
     float wm[kConsumers][4];   // per-warp running max per head (log2 units)
     float wl[kConsumers][4];   // per-warp softmax denominator per head
     int abort_flag;
     int next_page;             // next page index a consumer warp takes
     int tagK[kNK], tagV[kNV];  // page index each slot's latest fill holds (-1: none)
-    int is_last;
 };
-constexpr int kScratchBytes = 2 * 4 * kMaxSplits * 4;          // the split combine's weights
 constexpr int kPTabBytes = 2 * 128 * 4;                        // scale tables (see decode_kernel)
-constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kScratchBytes + kPTabBytes;
+constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kPTabBytes;
 static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
-static_assert(sizeof(Ctl) % 16 == 0, "the scratch after Ctl must stay 16-byte aligned");
-static_assert(4 * kMaxSplits * kPartStride * 4 <= kRingBytes, "the combine stages a head group's partials in the ring");
-static_assert(2 * 4 * kMaxSplits * 4 <= kScratchBytes, "the combine's weights fit the scratch");
+static_assert(sizeof(Ctl) % 16 == 0, "the tables after Ctl must stay 16-byte aligned");
 static_assert(kMaxSplits <= 64, "the combine handles two splits per lane");
 
 __device__ __forceinline__ float ex2(float x) {
@@ -338,7 +335,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     const float tau = a.tau;
     // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c)
     // f16x2
-    const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
+    const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl));
     const uint32_t* ptab_sdc = reinterpret_cast<const uint32_t*>(ptab_rcp + 128);
     const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
     const int gs = g & 3;
@@ -656,96 +653,64 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
     }
 }
 
-// Merge every split of (b, kv head h) into out (run by the last CTA).  The
-// head group's partials, one contiguous block, are first staged into shared
-// memory by a single bulk (TMA) copy.  Warp hh then finds head hh's
-// maximum M over the splits (one warp-wide integer max of order-preserving
-// keys) and the weights w_s = 2^(m_s - M) and w_s l_s (0 for an empty
-// split), one split per lane; finally each of 128 threads sums 4
-// consecutive dims of one head, and the denominator, over the splits.
-__device__ void combine_splits(const DecodeArgs& a, int b, int h, uint8_t* smem) {
+// Merge the split partials of (sequence b, query head j) into out: one CTA
+// of 128 threads per (b, j), launched after the decode with programmatic
+// dependent launch.  The head's partials (one contiguous block of
+// nsplit + 1 records) are staged into shared memory with 16-byte
+// asynchronous copies; warp 0 finds the maximum M over the splits (one
+// integer warp reduction of order-preserving keys), the weights
+// w_s = 2^(m_s - M) (0 for an empty split) and the denominator sum w_s l_s;
+// thread d then sums w_s O_s[d].
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
+    __shared__ __align__(16) float sp[kMaxSplits * kPartStride];
+    __shared__ float sw[kMaxSplits];
+    __shared__ float sden;
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int bj = blockIdx.x;   // b * hq + j
     const int nsplit1 = a.nsplit + 1;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float* base = a.parts + (size_t)(b * a.hq + 4 * h) * nsplit1 * kPartStride;
-    float* sp = reinterpret_cast<float*>(smem);                 // [4][nsplit1][132] staged partials
-    float* sw = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl));   // [4][kMaxSplits] weights
-    float* swl = sw + 4 * kMaxSplits;                           // [4][kMaxSplits] weights x l
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
-    const uint32_t bytes = 4u * nsplit1 * kPartStride * 4u;    // a multiple of 16 (528-byte rows)
-    const uint32_t cbar = smem_u32(&ctl->cbar);
-    if (tid == 0) {
-        mbar_init(cbar, 1);
-        fence_mbar_init();
-        // the other splits' partials were written through the generic proxy
-        // (made visible by the ticket's acquire) and the ring was last used
-        // through it too; order both before the async-proxy copy
-        asm volatile("fence.proxy.async;" ::: "memory");
-        mbar_arrive_expect_tx(cbar, bytes);
-        bulk_g2s(smem_u32(sp), base, bytes, cbar);
-    }
-    __syncthreads();   // the barrier is initialised before anyone waits on it
-    const bool landed = mbar_wait_bounded(cbar, 0, kWaitLimitNs, nullptr);
-    if (!__syncthreads_and(landed)) {   // uniform: every thread leaves or none
-        if (tid == 0) record_error(a.err, BD_ERR_TIMEOUT);
-        if (!landed) (void)mbar_wait_bounded(cbar, 0, kWaitLimitNs, nullptr);   // let the copy land first
-        return;
-    }
-    if (warp < 4) {
-        const float* ph = sp + (size_t)warp * nsplit1 * kPartStride;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const float* base = a.parts + (size_t)bj * nsplit1 * kPartStride;
+    griddep_wait();   // the decode grid has completed: its partials are visible
+    for (int i = tid; i < nsplit1 * (kPartStride / 4); i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (tid < 32) {
         float m[2], l[2];
         uint32_t key = 0;   // order-preserving u32 key of the largest m with l > 0
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int sidx = lane + 32 * r;
-            m[r] = (sidx < nsplit1) ? ph[sidx * kPartStride] : -INFINITY;
-            l[r] = (sidx < nsplit1) ? ph[sidx * kPartStride + 1] : 0.0f;
+            m[r] = (sidx < nsplit1) ? sp[sidx * kPartStride] : -INFINITY;
+            l[r] = (sidx < nsplit1) ? sp[sidx * kPartStride + 1] : 0.0f;
             if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
         }
-        key = __reduce_max_sync(0xFFFFFFFFu, key);
+        key = __reduce_max_sync(kFull, key);
         const float M = (key == 0) ? -INFINITY : f32_from_order_key(key);
+        float den = 0.0f;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int sidx = lane + 32 * r;
             const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
-            if (sidx < nsplit1) {
-                sw[warp * kMaxSplits + sidx] = w;
-                swl[warp * kMaxSplits + sidx] = w * l[r];
-            }
+            if (sidx < nsplit1) sw[sidx] = w;
+            den = fmaf(w, l[r], den);
         }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+        if (lane == 0) sden = den;
     }
     __syncthreads();
-    if (tid < kD) {
-        const int hh = tid >> 5, d0 = (tid & 31) * 4;
-        const float* ph = sp + (size_t)hh * nsplit1 * kPartStride + 4 + d0;
-        const float* wh = sw + hh * kMaxSplits;
-        const float* wlh = swl + hh * kMaxSplits;
-        float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
-        float den0 = 0.0f, den1 = 0.0f;
-        int sidx = 0;
+    const float* ph = sp + 4 + tid;
+    float n0 = 0.0f, n1 = 0.0f;
+    int sidx = 0;
 #pragma unroll 4
-        for (; sidx + 1 < nsplit1; sidx += 2) {
-            const float w0 = wh[sidx], w1 = wh[sidx + 1];
-            const float4 v0 = *reinterpret_cast<const float4*>(ph + sidx * kPartStride);
-            const float4 v1 = *reinterpret_cast<const float4*>(ph + (sidx + 1) * kPartStride);
-            n0.x = fmaf(w0, v0.x, n0.x); n0.y = fmaf(w0, v0.y, n0.y);
-            n0.z = fmaf(w0, v0.z, n0.z); n0.w = fmaf(w0, v0.w, n0.w);
-            n1.x = fmaf(w1, v1.x, n1.x); n1.y = fmaf(w1, v1.y, n1.y);
-            n1.z = fmaf(w1, v1.z, n1.z); n1.w = fmaf(w1, v1.w, n1.w);
-            den0 += wlh[sidx];
-            den1 += wlh[sidx + 1];
-        }
-        if (sidx < nsplit1) {
-            const float w0 = wh[sidx];
-            const float4 v0 = *reinterpret_cast<const float4*>(ph + sidx * kPartStride);
-            n0.x = fmaf(w0, v0.x, n0.x); n0.y = fmaf(w0, v0.y, n0.y);
-            n0.z = fmaf(w0, v0.z, n0.z); n0.w = fmaf(w0, v0.w, n0.w);
-            den0 += wlh[sidx];
-        }
-        const float den = den0 + den1;
-        const float r = (den > 0.0f) ? 1.0f / den : 0.0f;
-        *reinterpret_cast<float4*>(a.out + ((size_t)b * a.hq + 4 * h + hh) * kD + d0) =
-            make_float4((n0.x + n1.x) * r, (n0.y + n1.y) * r, (n0.z + n1.z) * r, (n0.w + n1.w) * r);
+    for (; sidx + 1 < nsplit1; sidx += 2) {
+        n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
+        n1 = fmaf(sw[sidx + 1], ph[(sidx + 1) * kPartStride], n1);
     }
+    if (sidx < nsplit1) n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
+    const float den = sden;
+    a.out[(size_t)bj * kD + tid] = (den > 0.0f) ? (n0 + n1) * (1.0f / den) : 0.0f;
 }
 
 template <int FMT, int PM>
@@ -798,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
             // exact per-byte tables for the E4M3 scale byte bb: the correctly
             // rounded 1/sd and the f16x2 pair (sd/c, sd/c) for the probability
             // quantizer (exact: c is a power of two)
-            float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl) + kScratchBytes);
+            float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl));
             const uint32_t bb = threadIdx.x;
             const float sd = e4m3_value(bb);
             const float cc = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
@@ -855,26 +820,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         __syncthreads();   // (B) warp states and drained ring
         write_split_partial(a, part, smem, ctl);
     }
-
-    // ---------------- ticket: the last CTA of (b, h) merges all splits
-    // The CTA barrier orders every thread's partial writes before thread 0's
-    // release; the acquire half makes the other splits' partials visible to
-    // the last CTA, whose threads read them (through L2) after the barrier.
-    griddep_wait();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int ticket;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                     : "=r"(ticket)
-                     : "l"(&a.counters[b * a.hkv + h])
-                     : "memory");
-        ctl->is_last = (ticket == nsplit1 - 1);
-    }
-    __syncthreads();
-    if (ctl->is_last) {
-        combine_splits(a, b, h, smem);
-        if (threadIdx.x == 0) a.counters[b * a.hkv + h] = 0;
-    }
 }
 
 // ------------------------------------------------------ bounded-wait test --
@@ -918,10 +863,8 @@ void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_s
     *pages_per_split = pps;
 }
 
-size_t decode_counter_bytes(int B, int hkv) { return ((size_t)B * hkv * sizeof(int) + 255) / 256 * 256; }
-
-size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit) {
-    return decode_counter_bytes(B, hkv) + (size_t)B * hq * (nsplit + 1) * kPartStride * sizeof(float);
+size_t decode_ws_bytes(int B, int hq, int nsplit) {
+    return (size_t)B * hq * (nsplit + 1) * kPartStride * sizeof(float);
 }
 
 using DecodeFn = void (*)(DecodeArgs);
@@ -953,7 +896,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return e;
+    // the split combine, dependent on the decode grid
+    cfg.gridDim = dim3((unsigned)(a.B * a.hq));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 // ------------------------------------------- fixed scratch (no allocation) --
@@ -961,8 +910,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
 // bd_decode_attention_noalloc serves callers that cannot call cudaMalloc --
 // for example code running inside another framework's memory pool, a plugin
 // that is handed only its input and output buffers, or a process whose GPU
-// memory is reserved up front.  Its split tickets and split partials live in
-// this file-scope array instead of a caller workspace.  Every GPU that loads
+// memory is reserved up front.  Its split partials live in this file-scope
+// array instead of a caller workspace (nothing in it has to start at zero).  Every GPU that loads
 // the library holds the array until the process exits; every call shares it,
 // so calls that overlap on the GPU race.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];

@@ -50,7 +50,6 @@ struct DecodeArgs {
     const uint16_t* tail_k;
     const uint16_t* tail_v;
     float* out;
-    int* counters;            // [B][Hkv] split tickets (zero between calls)
     float* parts;             // [B][Hq][nsplit + 1][kPartStride]
     int* err;
     size_t qstride;
@@ -64,8 +63,7 @@ cudaError_t launch_query(const QueryArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);
 void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split);
-size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit);
-size_t decode_counter_bytes(int B, int hkv);
+size_t decode_ws_bytes(int B, int hq, int nsplit);
 
 // Fixed device scratch of bd_decode_attention_noalloc (see bd_decode.cu).
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;

@@ -159,16 +159,17 @@ def test_repeat_calls_deterministic():
     assert np.array_equal(a["out"], b["out"])
 
 
-def test_workspace_reuse_and_split_tickets():
-    """The split tickets in the workspace reset themselves: one zeroed
-    workspace serves many calls, layers and batch shapes."""
+def test_workspace_needs_no_initialization_and_is_reusable():
+    """The workspace holds only split partials, each written before it is
+    read: one workspace that starts as garbage serves many calls, layers and
+    batch shapes."""
     ctx = bd.Context(bd.make_config(num_layers=2))
     ws = None
     for rep, lens in enumerate(([16 + 128 * 20 + 5], [700, 16 + 128 * 9], [16 + 128 * 20 + 5])):
         c = cases.build(cases.Spec(lens=lens, seed=90 + rep), ctx=ctx)
         need = bd.decode_workspace_size(ctx, 4, 64)
         if ws is None:
-            ws = torch.zeros(need // 4 + 1, dtype=torch.float32, device="cuda")
+            ws = torch.full((need // 4 + 1,), float("nan"), dtype=torch.float32, device="cuda")
         gpu = cases.run_gpu(c)
         ora = cases.run_oracle(c)
         mx, rl = cases.attn_errors(gpu["out"], ora["out"])
@@ -189,5 +190,4 @@ def test_workspace_reuse_and_split_tickets():
             bd.decode_attention(ctx, 0, qp, q, pool, bt, sl, *args, c.spec.tau, c.gk, c.gv, out, ws)
             torch.cuda.synchronize()
             assert np.array_equal(out.cpu().double().numpy(), gpu["out"])
-        assert int(ws[: 64].view(torch.int32).abs().sum()) == 0
     assert bd.read_device_error(ctx) == bd.OK
