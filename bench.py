@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-writer", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tau-sweep", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="also measure the 32K decode, the tau sweep at the default context, the 32-sequence batch "
+                         "(NVFP4 / MXFP4, recipe on / off) and the MXFP4 writer; attached as 'suite'")
     return ap.parse_args()
 
 
@@ -136,47 +139,76 @@ class ClockSampler:
 
 class DecodeWorkload:
     """Per-layer packed pools built by the library's own writer from seeded
-    bf16 K/V (generated per layer on the GPU and freed after packing)."""
+    bf16 K/V (generated per layer on the GPU and freed after packing).
 
-    def __init__(self, ctx_len, layers, tau, device, seed=0):
+    lens: context lengths of the batch.  One sequence takes its pages in a
+    seeded shuffle of the pool; a batch takes them round-robin across the
+    sequences from one shared pool.  fmt / recipe select the scale format and
+    whether keys are rotated and centered."""
+
+    def __init__(self, lens, layers, tau, device, seed=0, fmt=0, recipe=True):
         import torch
         import nvfp4_kv_cache_bd_gb300 as bd
         from nvfp4_kv_cache_bd_gb300 import synth
+        if isinstance(lens, int):
+            lens = [lens]
         self.bd, self.torch = bd, torch
         self.layers, self.tau = layers, tau
-        self.ctx = bd.Context(bd.make_config(num_layers=layers))
-        n_sink, self.npages, n_tail = synth.split_tokens(ctx_len)
-        self.seq_lens = torch.tensor([ctx_len], dtype=torch.int32, device=device)
-        self.block_table = synth.page_permutation(self.npages, seed, device).view(1, -1).contiguous()
+        self.B = B = len(lens)
+        self.ctx = bd.Context(bd.make_config(num_layers=layers, format=fmt, rotation=int(recipe),
+                                             centering=int(recipe)))
+        splits = [synth.split_tokens(L) for L in lens]
+        npg = [s_[1] for s_ in splits]
+        self.npages = sum(npg)
+        maxb = max([1] + npg)
+        self.seq_lens = torch.tensor(lens, dtype=torch.int32, device=device)
+        if B == 1:
+            bt = synth.page_permutation(self.npages, seed, device).view(1, -1).contiguous()
+        else:
+            rows = [[0] * maxb for _ in range(B)]
+            nxt = 0
+            for rnd in range(maxb):
+                for b in range(B):
+                    if rnd < npg[b]:
+                        rows[b][rnd] = nxt
+                        nxt += 1
+            bt = torch.tensor(rows, dtype=torch.int32, device=device)
+        self.block_table = bt
+        dst = torch.cat([bt[b, :npg[b]] for b in range(B)]) if self.npages else bt.new_zeros(0)
         self.rec = self.ctx.record_bytes
         self.pools, self.sinks, self.tails, self.gscales, self.qs = [], [], [], [], []
         for l in range(layers):
             lseed = 1000 * seed + l
             mu, mask = synth.key_mean(HKV, lseed, device)
-            k, v = synth.keys_values(ctx_len, HKV, lseed, device, mu=mu, mask=mask)
-            gk, gv = synth.gscales(k, v, mu, True, True)
+            kv = [synth.keys_values(L, HKV, lseed if B == 1 else 64 * lseed + b, device, mu=mu, mask=mask)
+                  for b, L in enumerate(lens)]
+            gk, gv = synth.gscales(torch.cat([x[0] for x in kv]), torch.cat([x[1] for x in kv]), mu, recipe,
+                                   recipe)
             bd.set_key_shift(self.ctx, l, mu)
-            pool = torch.empty(self.ctx.pool_bytes(self.npages), dtype=torch.uint8, device=device)
-            kp = k[16:16 + 128 * self.npages].view(self.npages, 128, HKV, D)
-            vp = v[16:16 + 128 * self.npages].view(self.npages, 128, HKV, D)
-            bd.quantize_kv_pages(self.ctx, l, kp, vp, self.block_table[0], gk, gv, pool)
-            sk = torch.zeros(1, 16, HKV, D, dtype=torch.bfloat16, device=device)
+            pool = torch.empty(self.ctx.pool_bytes(max(1, self.npages)), dtype=torch.uint8, device=device)
+            if self.npages:
+                kp = torch.cat([k[16:16 + 128 * n].view(n, 128, HKV, D) for (k, _), n in zip(kv, npg)])
+                vp = torch.cat([v[16:16 + 128 * n].view(n, 128, HKV, D) for (_, v), n in zip(kv, npg)])
+                bd.quantize_kv_pages(self.ctx, l, kp, vp, dst, gk, gv, pool)
+                del kp, vp
+            sk = torch.zeros(B, 16, HKV, D, dtype=torch.bfloat16, device=device)
             sv = torch.zeros_like(sk)
-            sk[0, :n_sink], sv[0, :n_sink] = k[:n_sink], v[:n_sink]
-            tk = torch.zeros(1, 128, HKV, D, dtype=torch.bfloat16, device=device)
+            tk = torch.zeros(B, 128, HKV, D, dtype=torch.bfloat16, device=device)
             tv = torch.zeros_like(tk)
-            tk[0, :n_tail], tv[0, :n_tail] = k[16 + 128 * self.npages:], v[16 + 128 * self.npages:]
+            for b, ((n_sink, n, n_tail), (k, v)) in enumerate(zip(splits, kv)):
+                sk[b, :n_sink], sv[b, :n_sink] = k[:n_sink], v[:n_sink]
+                tk[b, :n_tail], tv[b, :n_tail] = k[16 + 128 * n:], v[16 + 128 * n:]
             self.pools.append(pool)
             self.sinks.append((sk, sv))
             self.tails.append((tk, tv))
             self.gscales.append((gk, gv))
-            self.qs.append(synth.query(1, HQ, lseed, device))
-            del k, v, kp, vp
+            self.qs.append(synth.query(B, HQ, lseed, device))
+            del kv
         torch.cuda.synchronize()
-        self.qp = [torch.empty(1, self.ctx.query_packed_bytes, dtype=torch.uint8, device=device)
+        self.qp = [torch.empty(B, self.ctx.query_packed_bytes, dtype=torch.uint8, device=device)
                    for _ in range(layers)]
-        self.out = [torch.empty(1, HQ, D, dtype=torch.float32, device=device) for _ in range(layers)]
-        self.ws = torch.zeros(bd.decode_workspace_size(self.ctx, 1, self.npages) // 4 + 1, dtype=torch.float32,
+        self.out = [torch.empty(B, HQ, D, dtype=torch.float32, device=device) for _ in range(layers)]
+        self.ws = torch.empty(bd.decode_workspace_size(self.ctx, B, maxb) // 4 + 1, dtype=torch.float32,
                               device=device)
         self.bytes_per_layer = self.npages * HKV * 2 * self.rec
 
@@ -429,6 +461,8 @@ def main():
         line["tau_sweep_us_per_step"] = tau_sweep
     if writer:
         line["writer"] = writer
+    if args.suite:
+        line["suite"] = run_suite(args, device, stream, torch, bd, pg, hbm_peak)
     if rank == 0 and not args.no_cpu_baseline:
         smp = OracleDecodeSample(args.ctx, 256)
         runs = [smp.run() for _ in range(3)]
@@ -466,15 +500,52 @@ def decode_traffic(args):
     return DECODE_TRAFFIC["bytes"]
 
 
+def step_rate(wl, steps, warmup, stream, torch, pg, hbm_peak):
+    """µs per step of a graphed decode step and its packed-KV bandwidth."""
+    ms = timed(graphed(lambda: wl.step(), torch), steps, warmup, stream, torch, pg)
+    gbs = wl.bytes_per_layer * wl.layers / (ms * 1e-3) / 1e9
+    return {"us_per_step": ms * 1000.0, "packed_kv_gbs": gbs, "frac_of_peak": gbs / hbm_peak}
+
+
+def run_suite(args, device, stream, torch, bd, pg, hbm_peak):
+    """The other decode configurations, each a full 36-layer step."""
+    from nvfp4_kv_cache_bd_gb300 import synth
+    steps, out = 100, {}
+    wl = DecodeWorkload(32768, args.layers, 1.0, device)
+    out["decode_32k_ctx"] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak)
+    del wl
+    torch.cuda.empty_cache()
+    wl = DecodeWorkload(args.ctx, args.layers, 1.0, device)
+    sweep = {}
+    for tau in (0.0, 0.5, 4.0, 448.0):
+        wl.tau = tau
+        sweep[str(tau)] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak)
+    out[f"decode_{args.ctx // 1024}k_ctx_tau_sweep"] = sweep
+    del wl
+    torch.cuda.empty_cache()
+    lens = synth.log_uniform_lengths(32, 1024, 65536, 0)
+    batch = {"lengths": "32 seqs, log-uniform in [1024, 65536], %d tokens in all" % sum(lens)}
+    for fmt, fname in ((0, "nvfp4"), (1, "mxfp4")):
+        for recipe in (True, False):
+            wl = DecodeWorkload(lens, args.layers, 1.0, device, fmt=fmt, recipe=recipe)
+            batch[f"{fname}_{'rotation_centering' if recipe else 'plain_keys'}"] = step_rate(
+                wl, steps, args.warmup, stream, torch, pg, hbm_peak)
+            del wl
+            torch.cuda.empty_cache()
+    out["decode_batch_32"] = batch
+    out["writer_mxfp4"] = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=1)
+    return out
+
+
 def wl_bytes_note(args):
     npages = (args.ctx - 16) // 128
     return npages * HKV * 2 * 9216
 
 
-def bench_writer(args, device, stream, torch, bd, pg, hbm_peak):
+def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0):
     from nvfp4_kv_cache_bd_gb300 import synth
     seqs, layers = 64, args.layers
-    ctx = bd.Context(bd.make_config(num_layers=layers))
+    ctx = bd.Context(bd.make_config(num_layers=layers, format=fmt))
     pools, ks, vs, gs = [], [], [], []
     dst = synth.page_permutation(seqs, 7, device)
     for l in range(layers):
@@ -508,7 +579,8 @@ def bench_writer(args, device, stream, torch, bd, pg, hbm_peak):
     call_bytes = seqs * 128 * HKV * D * 2 * 2 + seqs * HKV * 2 * ctx.record_bytes
     call_ms = statistics.mean(durs)
     tok = seqs * 128
-    return {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, NVFP4",
+    fmt_name = "NVFP4" if fmt == 0 else "MXFP4"
+    return {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, {fmt_name}",
             "tok_per_s": tok / (ms * 1e-3) * (pg.get_world_size() if pg is not None else 1),
             "ms_per_step": ms, "gpu_launches_per_step": layers,
             "roofline": {"bound": "hbm", "kernel": "writer_kernel", "achieved": call_bytes / (call_ms * 1e-3) / 1e9,

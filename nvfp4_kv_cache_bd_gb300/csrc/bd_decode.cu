@@ -58,6 +58,8 @@ constexpr int kThreads = (kConsumers + 2) * 32;
 constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
 constexpr int kNK = 6, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
 constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
+constexpr int kWavePages = 32;   // one-wave splits up to this many pages ...
+constexpr int kBatchPages = 16;  // ... else splits of this many (more if kMaxSplits needs it)
 constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages them in 22.7 KB
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
@@ -854,6 +856,11 @@ void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_s
     int ns = max(1, slots / units - 1);
     ns = max(1, min(ns, max(1, max_blocks)));
     int pps = max(1, (max_blocks + ns - 1) / ns);
+    // When one wave would give a split many pages (a batch of long and short
+    // sequences: the host does not know the lengths), use short splits
+    // instead: a split past its sequence's pages exits at once and the
+    // hardware scheduler spreads the rest over several waves.
+    if (pps > kWavePages) pps = max(kBatchPages, (max_blocks + kMaxSplits - 2) / (kMaxSplits - 1));
     ns = max(1, (max_blocks + pps - 1) / pps);
     if (ns > kMaxSplits - 1) {
         pps = (max_blocks + kMaxSplits - 2) / (kMaxSplits - 1);
