@@ -507,6 +507,45 @@ def step_rate(wl, steps, warmup, stream, torch, pg, hbm_peak):
     return {"us_per_step": ms * 1000.0, "packed_kv_gbs": gbs, "frac_of_peak": gbs / hbm_peak}
 
 
+def bench_append(args, device, stream, torch, bd, pg, hbm_peak):
+    """bd_append_kv for 64 sequences per layer: a step of 36 launches with no
+    page completed, and one where every sequence completes a page (once
+    every 128 decode steps)."""
+    from nvfp4_kv_cache_bd_gb300 import synth
+    B, layers = 64, args.layers
+    ctx = bd.Context(bd.make_config(num_layers=layers))
+    mu, _ = synth.key_mean(HKV, 6000, device)
+    st = []
+    for l in range(layers):
+        bd.set_key_shift(ctx, l, mu)
+        g = torch.Generator(device=device)
+        g.manual_seed(6000 + l)
+        st.append(dict(
+            sk=torch.randn(B, 16, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            sv=torch.randn(B, 16, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            tk=torch.randn(B, 128, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            tv=torch.randn(B, 128, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            kn=torch.randn(B, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            vn=torch.randn(B, HKV, D, generator=g, device=device).to(torch.bfloat16),
+            pool=torch.empty(ctx.pool_bytes(2 * B), dtype=torch.uint8, device=device)))
+    bt = torch.arange(2 * B, dtype=torch.int32, device=device).view(B, 2)
+    out = {}
+    for name, L in (("no_page_completed", 16 + 128 + 5), ("every_sequence_completes_a_page", 16 + 128 + 127)):
+        sl = torch.full((B,), L, dtype=torch.int32, device=device)
+
+        def step():
+            for l in range(layers):
+                t = st[l]
+                bd.append_kv(ctx, l, t["kn"], t["vn"], sl, bt, t["sk"], t["sv"], t["tk"], t["tv"], 1.0, 1.0,
+                             t["pool"])
+
+        ms = timed(graphed(step, torch), 100, args.warmup, stream, torch, pg)
+        out[name + "_us_per_step"] = ms * 1000.0
+    out["workload"] = f"{B} sequences x {layers} layers, one token each"
+    out["page_fill_tok_per_s"] = B * 128 / (out["every_sequence_completes_a_page_us_per_step"] * 1e-6)
+    return out
+
+
 def run_suite(args, device, stream, torch, bd, pg, hbm_peak):
     """The other decode configurations, each a full 36-layer step."""
     from nvfp4_kv_cache_bd_gb300 import synth
@@ -534,6 +573,7 @@ def run_suite(args, device, stream, torch, bd, pg, hbm_peak):
             torch.cuda.empty_cache()
     out["decode_batch_32"] = batch
     out["writer_mxfp4"] = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=1)
+    out["append"] = bench_append(args, device, stream, torch, bd, pg, hbm_peak)
     return out
 
 

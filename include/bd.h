@@ -166,6 +166,30 @@ int bd_quantize_kv_pages(bd_ctx* ctx, int layer, const void* k, const void* v,
  *   B = 0 is a no-op. */
 int bd_quantize_query(bd_ctx* ctx, int layer, const void* q, int B, void* q_packed, void* stream);
 
+/* Append one decode-step token per sequence to the hybrid cache and pack the
+ * FP4 page it completes ([arch] hybrid cache: BF16 sink and tail, frozen
+ * FP4 pages; kv-landlords quant_ab.py freeze-at-fill).  One launch:
+ *   k_new, v_new : bf16 [B][num_kv_heads][128], device: the new token.
+ *   seq_lens     : int32 [B], device: each sequence's length L BEFORE this
+ *                  token; the token takes position L.  Not modified: advance
+ *                  it by one before the next decode reads the token.
+ *   sink_k/v     : bf16 [B][16][num_kv_heads][128], device, updated in place
+ *                  (the token goes to row L when L < 16).
+ *   tail_k/v     : bf16 [B][128][num_kv_heads][128], device, updated in place
+ *                  (row (L-16) mod 128 otherwise).
+ *   block_table  : int32 [B][max_blocks], device.  When the token completes
+ *                  tail page p = (L-16) div 128 (its row is 127), the page's
+ *                  128 tokens are quantized into pool page block_table[b][p]
+ *                  exactly as bd_quantize_kv_pages would; a page whose slot
+ *                  lies beyond max_blocks is skipped and BD_ERR_INVALID_ARG is
+ *                  recorded in the device error word.
+ *   k/v_gscale, kv_pool : as bd_quantize_kv_pages.
+ * This kernel does not allow the next grid to launch early, so a following
+ * decode sees the packed page and the new rows. */
+int bd_append_kv(bd_ctx* ctx, int layer, const void* k_new, const void* v_new, const int32_t* seq_lens,
+                 const int32_t* block_table, int max_blocks, void* sink_k, void* sink_v, void* tail_k,
+                 void* tail_v, int B, float k_gscale, float v_gscale, void* kv_pool, void* stream);
+
 /* Workspace bytes bd_decode_attention needs for B sequences whose block
  * table rows hold max_blocks entries (0 if B == 0). */
 size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
@@ -197,8 +221,9 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  * partials once the decode grid has completed.
  * Ordering: the kernel may start reading kv_pool and block_table while the
  * preceding grid in the stream, if it allows programmatic early launch,
- * still runs (this library's query and decode kernels do); those inputs
- * must be final before that grid was launched.  q_packed, q, the sink and
+ * still runs (this library's query, decode and combine kernels do); those
+ * inputs must be written by work that completes before that grid starts
+ * (bd_quantize_kv_pages and bd_append_kv never allow early launch).  q_packed, q, the sink and
  * tail rows, out and ws are touched only after the preceding grid has
  * completed. */
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q,

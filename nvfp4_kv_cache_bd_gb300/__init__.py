@@ -43,7 +43,8 @@ def make_config(num_layers=1, num_q_heads=32, num_kv_heads=8, format=FORMAT_NVFP
 
 
 EXPORTS = ("bd_create", "bd_destroy", "bd_status_string", "bd_set_key_shift", "bd_record_bytes",
-           "bd_query_packed_bytes", "bd_quantize_kv_pages", "bd_quantize_query", "bd_decode_workspace_size",
+           "bd_query_packed_bytes", "bd_quantize_kv_pages", "bd_append_kv", "bd_quantize_query",
+           "bd_decode_workspace_size",
            "bd_decode_attention", "bd_decode_attention_noalloc", "bd_read_device_error",
            "bd_selftest_bounded_wait")
 
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "bd_record_bytes": (SZ, [P]),
             "bd_query_packed_bytes": (SZ, [P]),
             "bd_quantize_kv_pages": (I, [P, I, P, P, P, I, F, F, P, P]),
+            "bd_append_kv": (I, [P, I, P, P, P, P, I, P, P, P, P, I, F, F, P, P]),
             "bd_quantize_query": (I, [P, I, P, I, P, P]),
             "bd_decode_workspace_size": (SZ, [P, I, I]),
             "bd_decode_attention": (I, [P, I, P, P, P, P, I, P, P, P, P, P, I, F, F, F, P, P, SZ, P]),
@@ -160,6 +162,23 @@ def quantize_kv_pages(ctx: Context, layer: int, k, v, dst_pages, k_gscale: float
         _dev(kv_pool, "kv_pool", torch.uint8)
     _check(lib().bd_quantize_kv_pages(ctx.handle, layer, _ptr(k), _ptr(v), _ptr(dst_pages), n, k_gscale, v_gscale,
                                       _ptr(kv_pool), _stream(stream)), "bd_quantize_kv_pages")
+
+
+def append_kv(ctx: Context, layer: int, k_new, v_new, seq_lens, block_table, sink_k, sink_v, tail_k, tail_v,
+              k_gscale: float, v_gscale: float, kv_pool, stream=None):
+    """bd_append_kv: store each sequence's new token at position seq_lens[b]
+    and pack the tail page it completes into the pool."""
+    B = k_new.shape[0]
+    max_blocks = block_table.shape[1] if block_table is not None and block_table.dim() == 2 else 0
+    if B:
+        _dev(k_new, "k_new", torch.bfloat16)
+        _dev(v_new, "v_new", torch.bfloat16)
+        _dev(seq_lens, "seq_lens", torch.int32)
+        for t, nme in ((sink_k, "sink_k"), (sink_v, "sink_v"), (tail_k, "tail_k"), (tail_v, "tail_v")):
+            _dev(t, nme, torch.bfloat16)
+    _check(lib().bd_append_kv(ctx.handle, layer, _ptr(k_new), _ptr(v_new), _ptr(seq_lens), _ptr(block_table),
+                              max_blocks, _ptr(sink_k), _ptr(sink_v), _ptr(tail_k), _ptr(tail_v), B, k_gscale,
+                              v_gscale, _ptr(kv_pool), _stream(stream)), "bd_append_kv")
 
 
 def quantize_query(ctx: Context, layer: int, q, q_packed, stream=None):

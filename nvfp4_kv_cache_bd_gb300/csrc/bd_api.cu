@@ -143,6 +143,47 @@ int bd_quantize_kv_pages(bd_ctx* ctx, int layer, const void* k, const void* v, c
     return cuda_status(bd::launch_writer(a, static_cast<cudaStream_t>(stream)));
 }
 
+int bd_append_kv(bd_ctx* ctx, int layer, const void* k_new, const void* v_new, const int32_t* seq_lens,
+                 const int32_t* block_table, int max_blocks, void* sink_k, void* sink_v, void* tail_k, void* tail_v,
+                 int B, float k_gscale, float v_gscale, void* kv_pool, void* stream) {
+    if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers || B < 0 || B > (1 << 20)) return BD_ERR_INVALID_ARG;
+    if (max_blocks < 0 || max_blocks > (1 << 22)) return BD_ERR_INVALID_ARG;
+    if (!finite_in(k_gscale, 1e-30f, 1e30f) || !finite_in(v_gscale, 1e-30f, 1e30f)) return BD_ERR_INVALID_ARG;
+    if (B == 0) return BD_OK;
+    if (!k_new || !v_new || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v) return BD_ERR_INVALID_ARG;
+    if (max_blocks > 0 && (!block_table || !kv_pool)) return BD_ERR_INVALID_ARG;
+    const uintptr_t align = (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)sink_k | (uintptr_t)sink_v |
+                            (uintptr_t)tail_k | (uintptr_t)tail_v | (uintptr_t)kv_pool;
+    if (align & 15u) return BD_ERR_INVALID_ARG;
+    int st = ensure_device(ctx);
+    if (st != BD_OK) return st;
+    bd::WriterArgs a;
+    a.k = static_cast<const uint16_t*>(tail_k);
+    a.v = static_cast<const uint16_t*>(tail_v);
+    a.dst_pages = nullptr;
+    a.mu = layer_mu(ctx, layer);
+    a.pool = static_cast<uint8_t*>(kv_pool);
+    a.n = B;
+    a.hkv = ctx->cfg.num_kv_heads;
+    a.format = ctx->cfg.format;
+    a.key_search = ctx->cfg.key_search;
+    a.rotation = ctx->cfg.rotation;
+    a.centering = ctx->cfg.centering;
+    a.gk = k_gscale;
+    a.gv = v_gscale;
+    a.seq_lens = seq_lens;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    a.sink_k = static_cast<uint16_t*>(sink_k);
+    a.sink_v = static_cast<uint16_t*>(sink_v);
+    a.tail_k = static_cast<uint16_t*>(tail_k);
+    a.tail_v = static_cast<uint16_t*>(tail_v);
+    a.err = ctx->d_err;
+    return cuda_status(bd::launch_writer(a, static_cast<cudaStream_t>(stream)));
+}
+
 int bd_quantize_query(bd_ctx* ctx, int layer, const void* q, int B, void* q_packed, void* stream) {
     if (!ctx || layer < 0 || layer >= ctx->cfg.num_layers || B < 0 || B > (1 << 20)) return BD_ERR_INVALID_ARG;
     if (B == 0) return BD_OK;

@@ -29,6 +29,20 @@ struct WriterArgs {
     uint8_t* pool;
     int n, hkv, format, key_search, rotation, centering;
     float gk, gv;
+    // Append mode (bd_append_kv) when seq_lens is set: n = B sequences, k/v
+    // are the BF16 tail buffers [B][128][Hkv][128]; the new token is stored
+    // at position seq_lens[b] and the tail page it completes is packed into
+    // block_table[b][(L - 16) / 128].
+    const int32_t* seq_lens = nullptr;
+    const int32_t* block_table = nullptr;
+    int max_blocks = 0;
+    const uint16_t* k_new = nullptr;   // [B][Hkv][128]
+    const uint16_t* v_new = nullptr;
+    uint16_t* sink_k = nullptr;        // [B][16][Hkv][128]
+    uint16_t* sink_v = nullptr;
+    uint16_t* tail_k = nullptr;        // [B][128][Hkv][128] (the same buffers as k, v)
+    uint16_t* tail_v = nullptr;
+    int* err = nullptr;
 };
 
 struct QueryArgs {

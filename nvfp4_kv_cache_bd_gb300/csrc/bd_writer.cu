@@ -333,14 +333,43 @@ __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) w
     const int kv = blockIdx.y;
     const int row0 = kCtaRows * blockIdx.z;            // first token of this CTA's half page
     const int grp = (row0 >> 4) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    const int64_t page = a.dst_pages[pg];
-    uint8_t* rec = a.pool + ((page * a.hkv + h) * 2 + kv) * (int64_t)record_bytes(a.format);
     const size_t tok_stride = (size_t)a.hkv * kD;
+    int64_t page;
+    const uint16_t* newrow = nullptr;   // append mode: the new token's row, staged as the page's last row
+    if (a.seq_lens) {
+        // append the token at position L (pg is the sequence) ...
+        const int L = a.seq_lens[pg];
+        const uint16_t* nrow = (kv == 0 ? a.k_new : a.v_new) + ((size_t)pg * a.hkv + h) * kD;
+        if (L < kSink) {
+            uint16_t* dst = (kv == 0 ? a.sink_k : a.sink_v) + (((size_t)pg * kSink + L) * a.hkv + h) * kD;
+            if (blockIdx.z == 0 && threadIdx.x < 16)
+                reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(nrow)[threadIdx.x];
+            return;
+        }
+        const int r = (L - kSink) % kPage, p = (L - kSink) / kPage;
+        if (r / kCtaRows == (int)blockIdx.z && threadIdx.x < 16) {
+            uint16_t* dst = (kv == 0 ? a.tail_k : a.tail_v) + (((size_t)pg * kPage + r) * a.hkv + h) * kD;
+            reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(nrow)[threadIdx.x];
+        }
+        // ... and pack the tail page it completes
+        if (r != kPage - 1) return;
+        if (p >= a.max_blocks) {
+            if (threadIdx.x == 0 && kv == 0 && blockIdx.z == 0) record_error(a.err, BD_ERR_INVALID_ARG);
+            return;
+        }
+        page = a.block_table[(size_t)pg * a.max_blocks + p];
+        newrow = nrow;
+    } else {
+        page = a.dst_pages[pg];
+    }
+    uint8_t* rec = a.pool + ((page * a.hkv + h) * 2 + kv) * (int64_t)record_bytes(a.format);
     const uint16_t* src = (kv == 0 ? a.k : a.v) + (((size_t)pg * kPage + row0) * a.hkv + h) * kD;
     // stage the CTA's rows (256 B each) with coalesced 16-byte copies
     for (int q = threadIdx.x; q < kCtaRows * 16; q += blockDim.x) {
         const int row = q >> 4, ch = q & 15;
-        cp_async16(smem_u32(tile + row * kTilePitch + 16 * ch), src + (size_t)row * tok_stride + 8 * ch);
+        const uint16_t* from = (newrow && row0 + row == kPage - 1) ? newrow + 8 * ch
+                                                                     : src + (size_t)row * tok_stride + 8 * ch;
+        cp_async16(smem_u32(tile + row * kTilePitch + 16 * ch), from);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     float* stab = reinterpret_cast<float*>(tile + kTileBytes);

@@ -96,6 +96,27 @@ def test_null_and_range_arguments(L):
     assert L.bd_quantize_query(h, 0, None, 1, fake, s) == bd.ERR_INVALID_ARG
     assert L.bd_quantize_query(h, 0, fake, -2, fake, s) == bd.ERR_INVALID_ARG
     assert L.bd_quantize_query(h, 0, None, 0, None, s) == bd.OK
+    # append: null pointers, bad layer, unaligned buffers, bad g; B = 0 is a no-op
+    app = [h, 0, fake, fake, fake, fake, 4, fake, fake, fake, fake, 2, 1.0, 1.0, fake, s]
+    for i in (2, 3, 4, 7, 8, 9, 10):
+        bad = list(app)
+        bad[i] = None
+        assert L.bd_append_kv(*bad) == bd.ERR_INVALID_ARG
+    bad = list(app)
+    bad[1] = 2
+    assert L.bd_append_kv(*bad) == bd.ERR_INVALID_ARG
+    bad = list(app)
+    bad[9] = P(0x10008)
+    assert L.bd_append_kv(*bad) == bd.ERR_INVALID_ARG
+    bad = list(app)
+    bad[12] = math.nan
+    assert L.bd_append_kv(*bad) == bd.ERR_INVALID_ARG
+    bad = list(app)
+    bad[5] = None   # block_table missing while max_blocks > 0
+    assert L.bd_append_kv(*bad) == bd.ERR_INVALID_ARG
+    bad = list(app)
+    bad[11] = 0
+    assert L.bd_append_kv(*bad) == bd.OK
     # decode: tau must be finite and in [0, 448]
     ws_need = L.bd_decode_workspace_size(h, 1, 4)
     assert ws_need > 0
