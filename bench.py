@@ -247,6 +247,23 @@ def graphed(fn, torch):
     return g.replay
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself on one GPU): the job's
+    step time is its slowest replica's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def job_rate(per_step_units: float, ms_step: float, world: int) -> float:
+    """Whole-job throughput of weakly scaled replicas: every rank processes
+    per_step_units per step, and a step lasts the slowest rank's ms_step."""
+    return world * per_step_units / (ms_step * 1e-3)
+
+
 def timed(fn, steps, warmup, stream, torch, dist=None, clocks=None):
     for _ in range(warmup):
         fn()
@@ -390,10 +407,7 @@ def main():
     if err != bd.OK:
         raise RuntimeError(f"device error word: {bd.status_string(err)}")
     dec_ms = statistics.mean(durs)
-    if pg is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t)
+    ms = max_over_ranks(ms, pg, device)
     us_step = ms * 1000.0
     step_bytes = wl.bytes_per_layer * args.layers
     achieved = wl.bytes_per_layer / (dec_ms * 1e-3) / 1e9
@@ -413,10 +427,7 @@ def main():
         out_host.copy_(out_dev, non_blocking=True)
 
     e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg)
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t)
+    e2e_ms = max_over_ranks(e2e_ms, pg, device)
     h2d = q_host.numel() * q_host.element_size()
     d2h = out_host.numel() * out_host.element_size()
 
@@ -446,8 +457,8 @@ def main():
                    "l2": f"not flushed: each step streams {args.layers} distinct layers' pools "
                          f"({step_bytes / 1e9:.2f} GB) >> 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "packed_kv_gbs": step_bytes / (ms * 1e-3) / 1e9,
-        "packed_kv_frac_of_peak": step_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "packed_kv_gbs": job_rate(step_bytes, ms, world) / 1e9,
+        "packed_kv_frac_of_peak": job_rate(step_bytes, ms, world) / 1e9 / (hbm_peak * world),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (+ split combine)", "achieved": achieved,
                      "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": decode_traffic(args), "bytes_per_launch": wl_bytes_note(args)},
@@ -611,17 +622,13 @@ def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0):
             evs[l][1].record()
         torch.cuda.synchronize()
         durs += [a.elapsed_time(b) for a, b in evs]
-    if pg is not None:
-        t = torch.tensor([ms], device=device)
-        dist_max = __import__("torch.distributed", fromlist=["all_reduce"])
-        dist_max.all_reduce(t, op=dist_max.ReduceOp.MAX)
-        ms = float(t)
+    ms = max_over_ranks(ms, pg, device)
     call_bytes = seqs * 128 * HKV * D * 2 * 2 + seqs * HKV * 2 * ctx.record_bytes
     call_ms = statistics.mean(durs)
     tok = seqs * 128
     fmt_name = "NVFP4" if fmt == 0 else "MXFP4"
     return {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, {fmt_name}",
-            "tok_per_s": tok / (ms * 1e-3) * (pg.get_world_size() if pg is not None else 1),
+            "tok_per_s": job_rate(tok, ms, pg.get_world_size() if pg is not None else 1),
             "ms_per_step": ms, "gpu_launches_per_step": layers,
             "roofline": {"bound": "hbm", "kernel": "writer_kernel", "achieved": call_bytes / (call_ms * 1e-3) / 1e9,
                          "peak": hbm_peak, "unit": "GB/s", "frac": call_bytes / (call_ms * 1e-3) / 1e9 / hbm_peak,
