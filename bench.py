@@ -338,6 +338,55 @@ class OracleDecodeSample:
         return dt * 1e6 * (self.npages / self.sample_pages) * LAYERS, dt
 
 
+def _oracle_all_cores_worker(args):
+    """One process of the all-core oracle run: build a sample, wait for the
+    others, time one pass."""
+    ctx_len, pages, barrier = args
+    smp = OracleDecodeSample(ctx_len, pages)
+    barrier.wait()
+    t = time.perf_counter()
+    smp.run()
+    return time.perf_counter() - t
+
+
+def oracle_extra_baselines(ctx_len):
+    """More oracle timings on the host: the page-fill writer (1 thread), the
+    4096-token single-layer step (1 thread), and the decode sample run by
+    every host core at once (one process each, spawned)."""
+    import multiprocessing as mp
+    import numpy as np
+    import torch
+    import oracle
+    from nvfp4_kv_cache_bd_gb300 import synth
+    out = {}
+    cfg = oracle.make_config()
+    pages = 16
+    mu, mask = synth.key_mean(HKV, 1)
+    k, v = synth.keys_values(128 * pages, HKV, 1, mu=mu, mask=mask)
+    u16 = lambda t: t.contiguous().view(torch.uint16).numpy()
+    pool = np.zeros(pages * HKV * 2 * oracle.record_bytes(cfg), np.uint8)
+    t = time.perf_counter()
+    oracle.quantize_kv_pages(cfg, u16(k.view(pages, 128, HKV, D)), u16(v.view(pages, 128, HKV, D)),
+                             np.arange(pages, dtype=np.int32), mu.numpy(), 1.0, 1.0, pool)
+    dt = time.perf_counter() - t
+    out["writer_tok_per_s_1core"] = pages * 128 / dt
+    smp0 = OracleDecodeSample(4096, 31)
+    out["step_4096_ctx_1_layer_us_1core"] = smp0.run()[1] * 1e6
+    ncores = max(1, os.cpu_count() or 1)
+    spages = 64
+    c = mp.get_context("spawn")
+    barrier = c.Manager().Barrier(ncores)
+    with c.Pool(ncores) as pool_:
+        dts = pool_.map(_oracle_all_cores_worker, [(ctx_len, spages, barrier)] * ncores)
+    npages = synth.split_tokens(ctx_len)[1]
+    out["decode_step_us_all_cores"] = max(dts) / ncores * 1e6 * (npages / spages) * LAYERS
+    out["all_cores"] = ncores
+    out["all_cores_sample"] = (f"{ncores} processes at once, each the oracle query + decode over {spages} of {npages} "
+                               "pages of one layer; step time = slowest process / processes, scaled to all pages "
+                               f"and {LAYERS} layers")
+    return out
+
+
 # -------------------------------------------------------------- reference --
 
 def run_reference(args):
@@ -480,6 +529,7 @@ def main():
         line["cpu_baseline"] = {"value": statistics.median(r[0] for r in runs), "unit": "µs/step", "cores": 1,
                                 "kind": "oracle",
                                 "sample": smp.describe() + f"; median of 3 runs of {runs[0][1]:.1f} s"}
+        line["cpu_baseline"].update(oracle_extra_baselines(args.ctx))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
