@@ -55,7 +55,10 @@
  *      scales[128 tokens][nb]: scale byte of block b of that token.
  *    The V record pairs token tau = 16 i + p with token tau + 8
  *    (16-token group i = 0..7, p = 0..7):
- *      codes [8 i][8 p][128 d]: byte = code(tau, d) | code(tau + 8, d) << 4.
+ *      codes [8 i][8 p][8 slots][16 B]: the byte of head dim d is
+ *        code(tau, d) | code(tau + 8, d) << 4, at slot (d/16) XOR 2(p mod 4),
+ *        byte d mod 16 of the slot.  (The XOR spreads the 16-byte reads of
+ *        the decode's P V fragments over all shared-memory banks.)
  *      scales[8 i][8 p][nb][2]: scale bytes of block b, token tau first.
  *    FP4 page p of a sequence holds its tokens 16 + 128 p ... 16 + 128 p + 127
  *    (tokens 0..15 are the BF16 sink).

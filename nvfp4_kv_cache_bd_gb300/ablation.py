@@ -49,8 +49,9 @@ SCHEMES = [
 # ------------------------------------------------------- host dequantizer --
 # Byte layouts of include/bd.h: a K record is codes[128 tok][64 B] (element
 # d of a token in byte d/2, even d in the low nibble) then scale bytes
-# [128 tok][nb]; a V record is codes[8][8][128 B] where byte d of row (i, p)
-# holds token 16i+p (low nibble) and token 16i+p+8 (high nibble), then
+# [128 tok][nb]; a V record is codes[8][8][128 B] where the byte of head dim
+# d in row (i, p) holds token 16i+p (low nibble) and token 16i+p+8 (high
+# nibble) and sits at 16-byte slot (d // 16) ^ 2 (p % 4), then
 # scales[8][8][nb][2].  nb = 8 E4M3 bytes (NVFP4) or 4 UE8M0 bytes (MXFP4).
 
 _E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, 0, -.5, -1, -1.5, -2, -3, -4, -6], np.float64)
@@ -81,7 +82,9 @@ def dequantize_pool(pool: np.ndarray, fmt: int, pages: np.ndarray, gk: float, gv
     kcodes = np.stack([kc & 0xF, kc >> 4], axis=-1).reshape(-1, H, 128, 128)
     ks = recs[:, :, 0, 8192:8192 + 128 * nb].reshape(-1, H, 128, nb)
     k = _E2M1[kcodes] * np.repeat(_scale(fmt, ks), 128 // nb, axis=-1)
-    vc = recs[:, :, 1, :8192].reshape(-1, H, 8, 8, 128)
+    vslot = recs[:, :, 1, :8192].reshape(-1, H, 8, 8, 8, 16)
+    p = np.arange(8)[:, None]
+    vc = vslot[:, :, :, p, np.arange(8)[None, :] ^ (2 * (p % 4))].reshape(-1, H, 8, 8, 128)
     vcodes = np.concatenate([vc & 0xF, vc >> 4], axis=3).reshape(-1, H, 128, 128)   # tokens 16i + (p | p+8)
     vs = recs[:, :, 1, 8192:8192 + 128 * nb].reshape(-1, H, 8, 8, nb, 2)
     vs = np.concatenate([vs[..., 0], vs[..., 1]], axis=3).reshape(-1, H, 128, nb)

@@ -1,6 +1,6 @@
 // Paged single-token decode attention over the hybrid cache (BF16 sink +
-// packed FP4 pages + BF16 tail): flash-decoding split-K over pages with the
-// split combine done by the last CTA of each (sequence, kv head).
+// packed FP4 pages + BF16 tail): flash-decoding split-K over pages, then a
+// separate kernel that merges the splits.
 //
 // Method: "How openbitsys/bitdecoding-fp4 works" (decode interface -> paged
 // attention kernel; hybrid cache); BitDecoding-FP4 evaluation config
@@ -8,27 +8,34 @@
 // probability_environment ("amax6" / "amax2_or_amax6" with c in {1, 8} and
 // tau in [0, 448]), RECIPE dual_residual_query_quantization (two query terms).
 //
-// Grid (nsplit + 1, kv heads, sequences), 160 threads.  Split 0 of a
-// (sequence, kv head) handles the BF16 sink and tail tokens with exact
-// probabilities; splits 1..nsplit each stream a contiguous range of that
-// sequence's FP4 pages.
+// Grid (nsplit + 1, kv heads, sequences) of 256-thread CTAs, two per SM.
+// Split 0 of a (sequence, kv head) attends the BF16 sink and tail tokens with
+// exact probabilities; split s >= 1 takes that sequence's FP4 pages
+// [(s - 1) * pages_per_split, s * pages_per_split).  The split-0 CTAs are
+// short: the SM slots they free early in a layer let the split combine and
+// the next layer's query and decode kernels become resident before this
+// decode ends, so the next decode's producers fill their rings during this
+// one's tail.
 //
-// FP4 split CTA: warp 4 is the producer; one elected lane streams each
-// page's K and V records (9216 B each in NVFP4) into a 6-stage shared-memory
-// ring with cp.async.bulk (TMA), completing on per-stage "full" mbarriers.
-// Warps 0..3 consume whole pages round-robin (page k -> warp k % 4), so a
-// page's softmax maximum never crosses warps and each warp carries eight
-// independent 16-token blocks through every phase:
+// FP4 split CTA: warps 6 and 7 are producers.  One lane of each streams the
+// pages' K records (warp 6) or V records (warp 7), in page order, into its
+// own 6-slot shared-memory ring with cp.async.bulk (TMA, L2 evict-first),
+// completing on per-slot "full" mbarriers; each slot carries the index of
+// the page it holds, so a consumer never mistakes an older fill for its own.
+// Warps 0..5 consume: each takes the next page from a shared counter, so
+// every warp's pages increase and a page's softmax maximum never crosses
+// warps.  Per page a warp carries eight 16-token blocks through
 //  QK  : m16n8k16 f16 MMAs, M = 16 tokens, N = 8 = 4 query heads x 2 query
 //        terms, K = 16 head dims.  FP4 codes are widened by cvt e2m1x2->f16x2
 //        and multiplied by their E4M3 scale in f16, which is exact
 //        (E2M1 x E4M3 has at most 6 significant bits and lies in
 //        [2^-10, 2688]); the query terms are exact the same way.  Per-tensor
 //        scales, the 1/sqrt(128) softmax scale and q.mu are applied to the
-//        fp32 accumulators.
+//        fp32 accumulators.  The K slot is released right after.
 //  P   : the page maximum m_p of every head (warp shuffles); P = exp(s - m_p);
 //        each 16-token block is quantized to FP4 with the amax2-or-amax6 rule;
-//        Phat = E2M1 x E4M3 / c is again exact in f16.
+//        Phat = E2M1 x E4M3 / c is again exact in f16.  All of this happens
+//        before the page's V record is awaited.
 //  PV  : O^T[128 dims][8] += Vhat^T[dims][16 tokens] Phat^T.  The V record
 //        stores tokens tau and tau+8 in one byte, which is exactly an
 //        A-fragment register of this MMA; Phat reaches the B-fragment layout
@@ -36,13 +43,13 @@
 //  Each warp merges its pages into a running (M, L, O); at the end the
 //  consumer warps' states are merged through shared memory into the split
 //  partial.
-// A second kernel, one CTA per (sequence, query head), merges the splits:
+// combine_kernel, one CTA per (sequence, query head), merges the splits:
 // O = sum 2^(m-M) O / sum 2^(m-M) l.
 //
-// Both are launched with programmatic dependent launch: the producers start
-// streaming pages while the query quantizer still runs; every thread that
-// reads the packed or raw query, or writes the workspace or out, first
-// waits on the preceding grid.
+// The query, decode and combine kernels use programmatic dependent launch:
+// the producers start streaming pages while the query quantizer still runs;
+// every thread that reads the packed or raw query or the sink/tail rows, or
+// writes the workspace or out, first waits on the preceding grid.
 #include <math.h>
 
 #include <mutex>
@@ -66,15 +73,19 @@ constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(
 struct alignas(16) Ctl {
     unsigned long long fullK[kNK], emptyK[kNK];   // K ring
     unsigned long long fullV[kNV], emptyV[kNV];   // V ring
-    float wm[kConsumers][4];   // per-warp running max per head (log2 units)
-    float wl[kConsumers][4];   // per-warp softmax denominator per head
+    float wm[kConsumers + 1][4];   // per-warp running max per head (log2 units); last: BF16 tokens
+    float wl[kConsumers + 1][4];   // per-warp softmax denominator per head
     int abort_flag;
     int next_page;             // next page index a consumer warp takes
     int tagK[kNK], tagV[kNV];  // page index each slot's latest fill holds (-1: none)
 };
 constexpr int kPTabBytes = 2 * 128 * 4;                        // scale tables (see decode_kernel)
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kPTabBytes;
-static_assert(2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes, "sink/tail staging must fit the ring");
+// Merge area in the (drained) ring: the O of each consumer warp and of the
+// BF16 tokens, [kConsumers + 1][4 heads][128] floats; the BF16 staging follows.
+constexpr int kStateBytes = (kConsumers + 1) * 4 * 128 * 4;
+static_assert(kStateBytes + 2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes,
+              "states and sink/tail staging must fit the ring");
 static_assert(sizeof(Ctl) % 16 == 0, "the tables after Ctl must stay 16-byte aligned");
 static_assert(kMaxSplits <= 64, "the combine handles two splits per lane");
 
@@ -171,29 +182,31 @@ __device__ __forceinline__ void max8_across_g(float* v, int lane) {
 constexpr int kRowPitch = 272;
 constexpr int kMaxBf16Tok = kSink + kPage - 1;   // 143
 
-__device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* part, uint8_t* smem) {
+// Attention of the 4 query heads of kv head h over the BF16 sink and tail
+// tokens of sequence b, left as state slot kConsumers of the CTA merge: O in
+// the merge area, the maximum and denominator in ctl (maximum -inf: no
+// tokens).  Runs on the whole CTA once the ring is no longer in use.
+__device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* smem, Ctl* ctl) {
     const int ns = min(L, kSink);
     const int rest = max(0, L - kSink);
     const int npages = rest / kPage;
     const int nt = rest - npages * kPage;
     const int T = ns + nt;
-    const int nsplit1 = a.nsplit + 1;
     const int tid = threadIdx.x;
     // the sink/tail rows and q may be produced by the preceding grid
     griddep_wait();
     if (T == 0) {
         if (tid < 4) {
-            part[tid * nsplit1 * kPartStride + 0] = -INFINITY;
-            part[tid * nsplit1 * kPartStride + 1] = 0.0f;
+            ctl->wm[kConsumers][tid] = -INFINITY;
+            ctl->wl[kConsumers][tid] = 0.0f;
         }
         return;
     }
-    uint8_t* ks = smem;                                            // [T][272 B] bf16 keys
+    float* so = reinterpret_cast<float*>(smem) + kConsumers * 4 * kD;   // this state's O
+    uint8_t* ks = smem + kStateBytes;                              // [T][272 B] bf16 keys
     uint8_t* vs = ks + kMaxBf16Tok * kRowPitch;                    // [T][272 B] bf16 values
     float* qf = reinterpret_cast<float*>(vs + kMaxBf16Tok * kRowPitch);   // [4][128]
     float* sp = qf + 4 * kD;                                       // [4][144] scores, then P
-    float* mh = sp + 4 * 144;                                      // [4]
-    float* lh = mh + 4;                                            // [4]
     // stage the sink and tail rows of this kv head with asynchronous 16-byte
     // copies (no thread waits for one load before issuing the next)
     for (int i = tid; i < T * 16; i += blockDim.x) {
@@ -218,23 +231,41 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    // scores: one thread per token, four heads
-    for (int tau = tid; tau < T; tau += blockDim.x) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-        for (int c = 0; c < 16; ++c) {
-            const uint4 u = *reinterpret_cast<const uint4*>(ks + tau * kRowPitch + 16 * c);
-            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+    // scores: two threads per token, four heads.  Thread half hf takes the
+    // 16-byte chunks 4hf..4hf+3 and 8+4hf..8+4hf+3 of the row, so the eight
+    // lanes of a quarter warp (four tokens, both halves) read distinct banks.
+    // The loop bound is the same for the whole CTA (every lane reaches the
+    // pair shuffle); a thread past the last token reads row T-1 and stores
+    // nothing.
+    {
+        const int hf = tid & 1;
+        for (int base = 0; base < T; base += blockDim.x >> 1) {
+            const int tau = base + (tid >> 1);
+            const int row = min(tau, T - 1);
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float k0 = bf16_lo(wd[e]), k1 = bf16_hi(wd[e]);
-                const int d = 8 * c + 2 * e;
+            for (int cc = 0; cc < 8; ++cc) {
+                const int c = (cc & 3) + 4 * hf + 8 * (cc >> 2);
+                const uint4 u = *reinterpret_cast<const uint4*>(ks + row * kRowPitch + 16 * c);
+                const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) s[hh] = fmaf(qf[hh * kD + d + 1], k1, fmaf(qf[hh * kD + d], k0, s[hh]));
+                for (int e = 0; e < 4; ++e) {
+                    const float k0 = bf16_lo(wd[e]), k1 = bf16_hi(wd[e]);
+                    const int d = 8 * c + 2 * e;
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        const float2 qq = *reinterpret_cast<const float2*>(&qf[hh * kD + d]);
+                        s[hh] = fmaf(qq.y, k1, fmaf(qq.x, k0, s[hh]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) s[hh] += __shfl_xor_sync(kFull, s[hh], 1);
+            if (hf == 0 && tau < T) {
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) sp[hh * 144 + tau] = s[hh] * kSmLog2e;
             }
         }
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) sp[hh * 144 + tau] = s[hh] * kSmLog2e;
     }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31;
@@ -252,29 +283,25 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, float* pa
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
         if (lane == 0) {
-            mh[warp] = m;
-            lh[warp] = l;
+            ctl->wm[kConsumers][warp] = m;
+            ctl->wl[kConsumers][warp] = l;
         }
     }
     __syncthreads();
-    // O = P V: one thread per head dim, four heads
-    if (tid < kD) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // O = P V: thread (head dim d, head pair hp), all 256 threads
+    {
+        const int d = tid & (kD - 1), hp = tid >> 7;
+        const float* p0 = sp + (2 * hp) * 144;
+        const float* p1 = p0 + 144;
+        float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll 4
         for (int tau = 0; tau < T; ++tau) {
-            const float v = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(vs + tau * kRowPitch + 2 * tid)) << 16);
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) acc[hh] = fmaf(sp[hh * 144 + tau], v, acc[hh]);
+            const float v = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(vs + tau * kRowPitch + 2 * d)) << 16);
+            acc0 = fmaf(p0[tau], v, acc0);
+            acc1 = fmaf(p1[tau], v, acc1);
         }
-#pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-            float* ph = part + hh * nsplit1 * kPartStride;
-            ph[4 + tid] = acc[hh];
-            if (tid == 0) {
-                ph[0] = mh[hh];
-                ph[1] = lh[hh];
-            }
-        }
+        so[(2 * hp) * kD + d] = acc0;
+        so[(2 * hp + 1) * kD + d] = acc1;
     }
 }
 
@@ -546,8 +573,11 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         for (int i = 0; i < 8; ++i) {
             {
                 const uint32_t b01 = bfr[2 * i], b23 = bfr[2 * i + 1];
-                const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * g);
-                const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * g);
+                // dims 16g .. 16g+15 of pair rows t and t+4 sit at slot
+                // g ^ 2t: each quarter warp's eight 16-byte reads cover all
+                // 32 banks
+                const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * (g ^ (2 * t)));
+                const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * (g ^ (2 * t)));
                 uint32_t vs0, vs1;
                 if (FMT == BD_FORMAT_NVFP4) {
                     vs0 = e4m3x2_to_f16x2(lds16(Vs + kCodeBytes + ((i * 8 + t) * 8 + g) * 2));
@@ -624,21 +654,23 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     }
 }
 
-// CTA merge of the consumer warps' states into this split's partial.
+// CTA merge of the states (consumer warps, then the BF16 tokens) into this
+// split's partial; a state with maximum -inf holds nothing and is skipped.
 __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint8_t* smem, const Ctl* ctl) {
     const int tid = threadIdx.x;
     if (tid >= 128) return;
     const int hh = tid >> 5, d0 = (tid & 31) * 4;
-    const int nsplit1 = a.nsplit + 1;
+    const int nparts = a.nsplit + 1;
     const float* sO = reinterpret_cast<const float*>(smem);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ctl->wm[w][hh]);
+    for (int w = 0; w <= kConsumers; ++w) M = fmaxf(M, ctl->wm[w][hh]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-        const float e = (ctl->wm[w][hh] == -INFINITY) ? 0.0f : ex2(ctl->wm[w][hh] - M);
+    for (int w = 0; w <= kConsumers; ++w) {
+        if (ctl->wm[w][hh] == -INFINITY) continue;
+        const float e = ex2(ctl->wm[w][hh] - M);
         const float4 v = *reinterpret_cast<const float4*>(&sO[(w * 4 + hh) * kD + d0]);
         acc.x = fmaf(e, v.x, acc.x);
         acc.y = fmaf(e, v.y, acc.y);
@@ -646,7 +678,7 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
         acc.w = fmaf(e, v.w, acc.w);
         L = fmaf(e, ctl->wl[w][hh], L);
     }
-    float* ph = part + hh * nsplit1 * kPartStride;
+    float* ph = part + hh * nparts * kPartStride;
     *reinterpret_cast<float4*>(&ph[4 + d0]) = acc;
     if ((tid & 31) == 0) {
         const bool aborted = ctl->abort_flag != 0 || M == -INFINITY;
@@ -669,11 +701,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     __shared__ float sden;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int bj = blockIdx.x;   // b * hq + j
-    const int nsplit1 = a.nsplit + 1;
+    const int nparts = a.nsplit + 1;   // partials per (sequence, query head)
     const int tid = threadIdx.x, lane = tid & 31;
-    const float* base = a.parts + (size_t)bj * nsplit1 * kPartStride;
+    const float* base = a.parts + (size_t)bj * nparts * kPartStride;
     griddep_wait();   // the decode grid has completed: its partials are visible
-    for (int i = tid; i < nsplit1 * (kPartStride / 4); i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
+    for (int i = tid; i < nparts * (kPartStride / 4); i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
@@ -683,8 +715,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int sidx = lane + 32 * r;
-            m[r] = (sidx < nsplit1) ? sp[sidx * kPartStride] : -INFINITY;
-            l[r] = (sidx < nsplit1) ? sp[sidx * kPartStride + 1] : 0.0f;
+            m[r] = (sidx < nparts) ? sp[sidx * kPartStride] : -INFINITY;
+            l[r] = (sidx < nparts) ? sp[sidx * kPartStride + 1] : 0.0f;
             if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
         }
         key = __reduce_max_sync(kFull, key);
@@ -694,7 +726,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
         for (int r = 0; r < 2; ++r) {
             const int sidx = lane + 32 * r;
             const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
-            if (sidx < nsplit1) sw[sidx] = w;
+            if (sidx < nparts) sw[sidx] = w;
             den = fmaf(w, l[r], den);
         }
 #pragma unroll
@@ -706,11 +738,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     float n0 = 0.0f, n1 = 0.0f;
     int sidx = 0;
 #pragma unroll 4
-    for (; sidx + 1 < nsplit1; sidx += 2) {
-        n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
-        n1 = fmaf(sw[sidx + 1], ph[(sidx + 1) * kPartStride], n1);
+    // an empty split wrote no O (its workspace bytes may hold anything, NaN
+    // included): it is skipped, not multiplied by its zero weight
+    for (; sidx + 1 < nparts; sidx += 2) {
+        const float w0 = sw[sidx], w1 = sw[sidx + 1];
+        if (w0 != 0.0f) n0 = fmaf(w0, ph[sidx * kPartStride], n0);
+        if (w1 != 0.0f) n1 = fmaf(w1, ph[(sidx + 1) * kPartStride], n1);
     }
-    if (sidx < nsplit1) n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
+    if (sidx < nparts && sw[sidx] != 0.0f) n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
     const float den = sden;
     a.out[(size_t)bj * kD + tid] = (den > 0.0f) ? (n0 + n1) * (1.0f / den) : 0.0f;
 }
@@ -720,8 +755,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     extern __shared__ __align__(128) uint8_t smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int L = a.seq_lens[b];
-    const int nsplit1 = a.nsplit + 1;
-    float* part = a.parts + ((size_t)(b * a.hq + 4 * h) * nsplit1 + split) * kPartStride;
+    float* part = a.parts + ((size_t)(b * a.hq + 4 * h) * (a.nsplit + 1) + split) * kPartStride;
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Let the next kernel in the stream launch now: this kernel reads the
@@ -732,17 +766,38 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
 
     // pages past the block-table row are ignored (the header bounds L)
     const int npages = min(max(0, L - kSink) / kPage, a.max_blocks);
-    const int p0 = (split - 1) * a.pages_per_split;
-    const int p1 = min(p0 + a.pages_per_split, npages);
+    const bool bf16 = split == 0;   // the BF16 sink and tail tokens, no FP4 pages
+    const int p0 = bf16 ? 0 : (split - 1) * a.pages_per_split;
+    const int p1 = bf16 ? 0 : min(p0 + a.pages_per_split, npages);
 
-    if (split == 0) {
-        bf16_segment(a, b, h, L, part, smem);
-    } else if (p0 >= p1) {
+    if (bf16) {
+        // warm L2 with this head's sink and tail rows while the preceding
+        // grid drains (a hint: nothing is read here, so it may run before
+        // the dependency wait)
+        const int ns = min(L, kSink), rest = max(0, L - kSink), nt = rest - (rest / kPage) * kPage;
+        for (int i = threadIdx.x; i < 2 * (ns + nt); i += blockDim.x) {
+            const int tau = i >> 1;
+            const size_t row = tau < ns ? (((size_t)b * kSink + tau) * a.hkv + h) * kD
+                                        : (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
+            const uint16_t* base = tau < ns ? ((i & 1) ? a.sink_v : a.sink_k) : ((i & 1) ? a.tail_v : a.tail_k);
+            bulk_prefetch_l2(base + row, kD * 2);
+        }
+    }
+    if (p0 >= p1 && !bf16) {
         griddep_wait();
         if (threadIdx.x < 4) {
-            part[threadIdx.x * nsplit1 * kPartStride + 0] = -INFINITY;
-            part[threadIdx.x * nsplit1 * kPartStride + 1] = 0.0f;
+            part[threadIdx.x * (a.nsplit + 1) * kPartStride + 0] = -INFINITY;
+            part[threadIdx.x * (a.nsplit + 1) * kPartStride + 1] = 0.0f;
         }
+        return;
+    }
+    if (p0 >= p1) {
+        // no FP4 pages: the consumer states are empty and nothing aborted
+        if (threadIdx.x < kConsumers * 4) {
+            ctl->wm[threadIdx.x >> 2][threadIdx.x & 3] = -INFINITY;
+            ctl->wl[threadIdx.x >> 2][threadIdx.x & 3] = 0.0f;
+        }
+        if (threadIdx.x == 0) ctl->abort_flag = 0;
     } else {
         const int n = p1 - p0;
         constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
@@ -819,9 +874,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         } else {
             consume_pages<FMT, PM>(a, b, h, n, smem, ctl, warp, lane);   // contains (A)
         }
-        __syncthreads();   // (B) warp states and drained ring
-        write_split_partial(a, part, smem, ctl);
     }
+    if (!bf16 && threadIdx.x < 4) {
+        ctl->wm[kConsumers][threadIdx.x] = -INFINITY;
+        ctl->wl[kConsumers][threadIdx.x] = 0.0f;
+    }
+    __syncthreads();   // (B) warp states and drained ring
+    if (bf16) bf16_segment(a, b, h, L, smem, ctl);   // the same for the whole CTA
+    __syncthreads();
+    write_split_partial(a, part, smem, ctl);
 }
 
 // ------------------------------------------------------ bounded-wait test --

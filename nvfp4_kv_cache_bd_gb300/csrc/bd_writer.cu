@@ -287,7 +287,9 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, int row0,
     const int t0 = 16 * grp + p, t1 = t0 + 8;
     const uint8_t* r0 = tile + (t0 - row0) * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
     const uint8_t* r1 = tile + (t1 - row0) * kTilePitch + 64 * c;
-    uint8_t* codes = rec + (grp * 8 + p) * kD + 32 * c;
+    // dims 32c .. 32c+31 are 16-byte slots 2c, 2c+1, stored at slots
+    // 2c XOR 2(p mod 4) and the one after it
+    uint8_t* codes = rec + (grp * 8 + p) * kD + 32 * (c ^ (p & 3));
     uint32_t words[8];
     if (FMT == BD_FORMAT_NVFP4) {
         // one 16-dim block of both tokens at a time

@@ -300,13 +300,19 @@ static void put_k(const or_config* c, uint8_t* rec, int tok, const uint8_t* code
 }
 
 /* V record: tokens are paired (tau, tau+8) inside each 16-token group i
- * (tau = 16 i + p, p = 0..7).  codes[i][p][d] holds token tau in the low
- * nibble and token tau+8 in the high nibble; scales[i][p][b][2] holds the
- * two tokens' scale bytes of block b, token tau first. */
+ * (tau = 16 i + p, p = 0..7).  Row (i, p) is 128 bytes: the byte of head
+ * dim d holds token tau in the low nibble and token tau+8 in the high
+ * nibble, and the 16 bytes of dims 16c..16c+15 sit at 16-byte slot
+ * c XOR 2(p mod 4) of the row.  scales[i][p][b][2] holds the two tokens'
+ * scale bytes of block b, token tau first. */
+static int v_code_off(int i, int p, int d) {
+    return (i * 8 + p) * OR_D + (((d >> 4) ^ (2 * (p & 3))) << 4) + (d & 15);
+}
+
 static void put_v(const or_config* c, uint8_t* rec, int tok, const uint8_t* codes128, const uint8_t* sbs) {
     int i = tok / 16, r = tok % 16, p = r % 8, hi = r / 8;
     for (int d = 0; d < OR_D; d++) {
-        uint8_t* byte = &rec[(i * 8 + p) * OR_D + d];
+        uint8_t* byte = &rec[v_code_off(i, p, d)];
         if (hi) *byte = (uint8_t)((*byte & 0x0F) | ((codes128[d] & 0xF) << 4));
         else *byte = (uint8_t)((*byte & 0xF0) | (codes128[d] & 0xF));
     }
@@ -322,7 +328,7 @@ static uint8_t get_k_scale(const or_config* c, const uint8_t* rec, int tok, int 
 }
 static uint8_t get_v_code(const uint8_t* rec, int tok, int d) {
     int i = tok / 16, r = tok % 16, p = r % 8, hi = r / 8;
-    uint8_t byte = rec[(i * 8 + p) * OR_D + d];
+    uint8_t byte = rec[v_code_off(i, p, d)];
     return hi ? (byte >> 4) : (byte & 0xF);
 }
 static uint8_t get_v_scale(const or_config* c, const uint8_t* rec, int tok, int b) {

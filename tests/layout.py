@@ -3,8 +3,10 @@ oracle and of the CUDA path, from the layout the public header documents).
 
 K record (per page, KV head): codes[128 tok][64 B] (head-dim element d in
 byte d/2, even d in the low nibble), then scales[128 tok][nb].
-V record: codes[8 groups][8 pairs][128 d], byte = token 16i+p (low nibble)
-and token 16i+p+8 (high nibble); scales[8][8][nb][2] (token 16i+p first).
+V record: codes[8 groups][8 pairs][8 slots][16 B]; the byte of head dim d
+holds token 16i+p (low nibble) and token 16i+p+8 (high nibble) and sits at
+slot (d // 16) ^ 2 (p % 4), byte d % 16; scales[8][8][nb][2] (token 16i+p
+first).
 nb = 8 E4M3 bytes (NVFP4, 16-element blocks) or 4 UE8M0 bytes (MXFP4, 32).
 Pool: records ordered [page][kv_head][K, V].
 """
@@ -57,7 +59,11 @@ def k_record(fmt: int, rec: np.ndarray):
 def v_record(fmt: int, rec: np.ndarray):
     """Same as k_record for a V record (token order restored)."""
     nb = nblocks(fmt)
-    by = rec[:8192].reshape(8, 8, 128)
+    raw = rec[:8192].reshape(8, 8, 8, 16)
+    by = np.empty((8, 8, 128), np.uint8)
+    for p in range(8):
+        for c in range(8):
+            by[:, p, 16 * c:16 * c + 16] = raw[:, p, c ^ (2 * (p % 4))]
     codes = np.empty((128, 128), np.uint8)
     sbr = rec[8192:8192 + 128 * nb].reshape(8, 8, nb, 2)
     sb = np.empty((128, nb), np.uint8)

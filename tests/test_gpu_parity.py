@@ -17,6 +17,13 @@ pytestmark = pytest.mark.gpu
 MAX_ABS, REL_L2 = 2e-3, 1e-3
 
 
+def same_up_to_merge_order(x, y):
+    """Two decode outputs of the same inputs: finite and equal up to the fp32
+    rounding of the order in which a split merges its pages."""
+    assert np.isfinite(x).all() and np.isfinite(y).all()
+    np.testing.assert_allclose(x, y, rtol=2e-6, atol=1e-7)
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     from nvfp4_kv_cache_bd_gb300 import build
@@ -152,11 +159,38 @@ def test_bounded_wait_reports_timeout():
 
 
 def test_repeat_calls_deterministic():
-    c = cases.build(cases.Spec(lens=[16 + 128 * 4 + 9], seed=81))
+    """The writer and the query quantizer are bitwise deterministic.  The
+    decode's consumer warps take pages as they become free, so which warp
+    accumulates which page (and so the fp32 merge order of a split) varies
+    from call to call: outputs agree to fp32 rounding, not bit for bit."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 40 + 9], seed=81))
     a = cases.run_gpu(c)
     b = cases.run_gpu(c)
     assert np.array_equal(a["pool"], b["pool"]) and np.array_equal(a["qp"], b["qp"])
-    assert np.array_equal(a["out"], b["out"])
+    same_up_to_merge_order(a["out"], b["out"])
+
+
+def test_empty_splits_ignore_workspace_garbage():
+    """A batch whose short sequence leaves splits without pages, on a first
+    call into a workspace full of NaN: the empty splits' unwritten O must not
+    reach the output (the same result as with a zeroed workspace)."""
+    c = cases.build(cases.Spec(lens=[700, 16 + 128 * 9 + 3], seed=77))
+    gpu = cases.run_gpu(c)   # zeroed workspace
+    ora = cases.run_oracle(c)
+    mx, rl = cases.attn_errors(gpu["out"], ora["out"])
+    assert mx < MAX_ABS and rl < REL_L2
+    dev = "cuda"
+    bt = torch.from_numpy(c.block_table).to(dev)
+    B = bt.shape[0]
+    ws = torch.full((bd.decode_workspace_size(c.ctx, B, bt.shape[1]) // 4 + 1,), float("nan"),
+                    dtype=torch.float32, device=dev)
+    out = torch.full((B, 32, 128), float("nan"), device=dev)
+    bd.decode_attention(c.ctx, 0, torch.from_numpy(gpu["qp"]).to(dev), c.q.to(dev), torch.from_numpy(gpu["pool"]).to(dev),
+                        bt, torch.from_numpy(c.seq_lens).to(dev), *[x.to(dev) for x in (c.sink_k, c.sink_v, c.tail_k,
+                                                                                          c.tail_v)],
+                        c.spec.tau, c.gk, c.gv, out, ws)
+    torch.cuda.synchronize()
+    same_up_to_merge_order(out.cpu().double().numpy(), gpu["out"])
 
 
 def test_workspace_needs_no_initialization_and_is_reusable():
@@ -189,5 +223,5 @@ def test_workspace_needs_no_initialization_and_is_reusable():
             out = torch.full((B, 32, 128), float("nan"), device=dev)
             bd.decode_attention(ctx, 0, qp, q, pool, bt, sl, *args, c.spec.tau, c.gk, c.gv, out, ws)
             torch.cuda.synchronize()
-            assert np.array_equal(out.cpu().double().numpy(), gpu["out"])
+            same_up_to_merge_order(out.cpu().double().numpy(), gpu["out"])
     assert bd.read_device_error(ctx) == bd.OK
