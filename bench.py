@@ -513,8 +513,11 @@ def main():
                      "traffic": decode_traffic(args), "bytes_per_launch": wl_bytes_note(args)},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "µs/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * args.layers * 2,
-        "launch": "one CUDA graph per step (36 x query kernel + decode kernel, programmatic dependent launch)",
+        # per layer: the query kernel, then bd_decode_attention's decode and
+        # split-combine kernels
+        "gpu_launches": args.steps * args.layers * 3,
+        "launch": (f"one CUDA graph per step ({args.layers} x query, decode and split-combine kernels, "
+                   "programmatic dependent launch)"),
         "clocks": clk,
     }
     if tau_sweep:
@@ -542,7 +545,7 @@ def main():
 # run of this bench; a launch's traffic does not depend on the layer count.
 # Valid only for the kernel sources it was taken on: reported as null once
 # their hash differs.
-DECODE_TRAFFIC = {"sources_sha256_16": "dc5b596f14fa8a93", "ctx": 131072, "bytes": 151467776 + 3574272}
+DECODE_TRAFFIC = {"sources_sha256_16": "40168ad3a624d8a2", "ctx": 131072, "bytes": 151482112 + 3174144}
 DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h")
 
 
