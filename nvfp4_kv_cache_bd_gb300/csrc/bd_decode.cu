@@ -770,19 +770,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     const int p0 = bf16 ? 0 : (split - 1) * a.pages_per_split;
     const int p1 = bf16 ? 0 : min(p0 + a.pages_per_split, npages);
 
-    if (bf16) {
-        // warm L2 with this head's sink and tail rows while the preceding
-        // grid drains (a hint: nothing is read here, so it may run before
-        // the dependency wait)
-        const int ns = min(L, kSink), rest = max(0, L - kSink), nt = rest - (rest / kPage) * kPage;
-        for (int i = threadIdx.x; i < 2 * (ns + nt); i += blockDim.x) {
-            const int tau = i >> 1;
-            const size_t row = tau < ns ? (((size_t)b * kSink + tau) * a.hkv + h) * kD
-                                        : (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
-            const uint16_t* base = tau < ns ? ((i & 1) ? a.sink_v : a.sink_k) : ((i & 1) ? a.tail_v : a.tail_k);
-            bulk_prefetch_l2(base + row, kD * 2);
-        }
-    }
     if (p0 >= p1 && !bf16) {
         griddep_wait();
         if (threadIdx.x < 4) {
