@@ -31,6 +31,15 @@
  *
  * Readings where the pages are silent are listed in the repository's design
  * notes; each function below states the reading it implements.
+ *
+ * Pins: the CPU tests check every function here against something other than
+ * itself -- brute force over the code tables, closed forms, the explicit
+ * Sylvester matrix, textbook softmax attention in fp64 -- except the
+ * probability quantizer's reading of the pages (per-page reference maximum,
+ * amax2-or-amax6 by tau on u = c*P, the unquantized denominator).  That part
+ * is pinned only by its endpoints (tau = 0, tau = 448) and closed forms (all
+ * keys equal); beyond them its parity is unpinned, since the pages print no
+ * value to check it against.
  */
 #include <math.h>
 #include <stdint.h>
