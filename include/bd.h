@@ -86,7 +86,7 @@ extern "C" {
 enum {
     BD_OK = 0,
     BD_ERR_INVALID_ARG = -1,  /* null pointer, size out of range, non-finite or out-of-range scalar */
-    BD_ERR_UNSUPPORTED = -2,  /* a configuration this build does not implement */
+    BD_ERR_UNSUPPORTED = -2,  /* a configuration this library does not implement */
     BD_ERR_CUDA = -3,         /* a CUDA runtime call failed */
     BD_ERR_WORKSPACE = -4,    /* the caller's workspace is smaller than required */
     BD_ERR_TIMEOUT = -5       /* a bounded device-side wait ran out (reported via the error word) */
@@ -120,7 +120,7 @@ typedef struct bd_ctx bd_ctx;
 
 /* Validate cfg and create a context (host memory only; no CUDA call).
  * Returns BD_ERR_INVALID_ARG for null pointers or values out of range,
- * BD_ERR_UNSUPPORTED for head_dim / page_size / sink / GQA ratios this build
+ * BD_ERR_UNSUPPORTED for head_dim / page_size / sink / GQA ratios this library
  * does not implement.  *out is set only on success. */
 int bd_create(const bd_config* cfg, bd_ctx** out);
 
