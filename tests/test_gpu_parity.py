@@ -225,3 +225,29 @@ def test_workspace_needs_no_initialization_and_is_reusable():
             torch.cuda.synchronize()
             same_up_to_merge_order(out.cpu().double().numpy(), gpu["out"])
     assert bd.read_device_error(ctx) == bd.OK
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 448.0])
+def test_two_level_pages_use_each_pages_own_max(tau):
+    """The probability quantizer's reference maximum is each page's own
+    (reading A7): two FP4 pages whose keys are constant at two levels (page 1
+    holds half of page 0's key row; the sink holds page 0's row), values +1.5
+    and -1.5 on the pages and 0 in the sink.  The CPU pins show that the
+    oracle's output here is the per-page closed form and that a maximum over
+    both pages would miss it by more than five times this tolerance."""
+    c = cases.build(cases.Spec(lens=[16 + 2 * 128], seed=52, tau=tau))
+    kA = c.sink_k[0, 0].clone()
+    kB = (kA.float() * 0.5).to(torch.bfloat16)
+    c.sink_k[0] = kA
+    c.sink_v.zero_()
+    c.k_pages = torch.stack([kA.expand(128, 8, 128), kB.expand(128, 8, 128)]).contiguous()
+    vp = torch.empty(2, 128, 8, 128, dtype=torch.bfloat16)
+    vp[0], vp[1] = 1.5, -1.5
+    c.v_pages = vp
+    c.gv = 0.25
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c)
+    assert np.array_equal(gpu["pool"], ora["pool"])
+    mx, rl = cases.attn_errors(gpu["out"], ora["out"])
+    assert mx < MAX_ABS and rl < REL_L2, (mx, rl)
+    assert bd.read_device_error(c.ctx) == bd.OK

@@ -641,3 +641,104 @@ def test_empty_sequence_gives_zero():
     c = build_case(40, 71, cfg)
     c["seq_lens"] = np.zeros(1, np.int32)
     assert not run_oracle(cfg, c).any()
+
+
+def const_block_phat(u, mode, c):
+    """Phat of a 16-token block whose values u = c*P all equal u, written out
+    from the NVFP4 block steps with per-tensor scale 1: s = RN(u / mode), the
+    E4M3 scale sd nearest to s, code = E2M1(RN(u * RN(1/sd))), Phat =
+    value(code) * sd / c.  (Uses the brute-force encoders above.)"""
+    u = np.float32(u)
+    s = np.float32(u / np.float32(mode))
+    sd = layout.E4M3[brute_e4m3(np.array([s], np.float32))[0]]
+    if sd == 0.0:
+        return 0.0
+    inv = np.float32(1.0) / np.float32(sd)
+    code = brute_e2m1(np.array([np.float32(u * inv)], np.float32))[0]
+    return E2M1_MAG[code & 7] * sd / c
+
+
+def two_level_case(seed=52):
+    """Hybrid cache of 16 + 2*128 tokens: the sink and FP4 page 0 hold one
+    key row kA (per kv head) for every token, page 1 holds kB = kA / 2, so
+    every page's logits are constant but the two pages sit at different
+    levels.  Values: 0 in the sink, +1.5 on page 0 and -1.5 on page 1 (exact
+    in NVFP4 with g_V = 0.25: block scale 1, code 6), so the output is the
+    signed balance of the two pages' weights."""
+    cfg = oracle.make_config()          # NVFP4, amax2-or-amax6, c = 8
+    n = 2
+    L = 16 + 128 * n
+    c = build_case(L, seed, cfg)
+    kA = torch.from_numpy(c["sink_k"]).view(torch.bfloat16)[0, 0].clone()      # [Hkv][128]
+    kB = (kA.float() * 0.5).to(torch.bfloat16)
+    sink_k = torch.zeros(1, 16, 8, 128, dtype=torch.bfloat16)
+    sink_k[0] = kA
+    c["sink_k"] = sink_k.view(torch.uint16).numpy()
+    c["sink_v"] = np.zeros_like(c["sink_v"])
+    kp = torch.stack([kA.expand(128, 8, 128), kB.expand(128, 8, 128)]).contiguous()
+    vp = torch.empty(n, 128, 8, 128, dtype=torch.bfloat16)
+    vp[0], vp[1] = 1.5, -1.5
+    c["k_pages"], c["v_pages"] = kp, vp
+    c["gv"] = 0.25
+    c["pool"][:] = 0
+    oracle.quantize_kv_pages(cfg, kp.view(torch.uint16).numpy(), vp.view(torch.uint16).numpy(), c["bt"][0],
+                             c["mu"].numpy(), c["gk"], c["gv"], c["pool"])
+    c["kA"] = kA
+    return cfg, c
+
+
+def two_level_closed_forms(c, tau):
+    """Expected outputs [32][128] of the two-level case under the per-page
+    reference maximum, and under a maximum taken over both FP4 pages."""
+    sm = 1 / np.sqrt(128)
+    q = c["q"][0].double().numpy()
+    qhat = layout.query_record(0, 32, c["qp"][0])[0]
+    kA = c["kA"].double().numpy()
+    mode = 2 if 8.0 < tau else 6         # u = c * P = 8 on every token of a page
+    f = const_block_phat(8.0, mode, 8)
+    per_page = np.zeros((32, 128))
+    global_max = np.zeros((32, 128))
+    for j in range(32):
+        h = j // 4
+        s_bf = sm * q[j] @ kA[h]
+        s, vsum = [], []
+        for p in range(2):
+            kv = layout.k_record(0, layout.pool_record(c["pool"], 0, 8, c["bt"][0, p], h, 0))[2]
+            assert np.all(kv == kv[0])   # one key row per page
+            s.append(sm * (kv[0] @ qhat[j] * c["gk"] + q[j] @ c["mu"][h].double().numpy()))
+            vv = layout.v_record(0, layout.pool_record(c["pool"], 0, 8, c["bt"][0, p], h, 1))[2]
+            vsum.append(vv.sum(0) * c["gv"])
+        M = max(s_bf, *s)
+        wb = np.exp(s_bf - M)
+        w = [np.exp(x - M) for x in s]
+        num = sum(w[p] * f * vsum[p] for p in range(2))          # the sink's values are 0
+        den = wb * 16 + sum(w[p] * 128 for p in range(2))
+        per_page[j] = num / den
+        # the other reading: P = exp(s_p - max(s_0, s_1)) quantized block by block
+        mf = max(s)
+        wf = np.exp(mf - M)
+        pr = [np.exp(x - mf) for x in s]
+        ph = [const_block_phat(np.float32(8.0 * x), 2 if np.float32(8.0 * x) < tau else 6, 8) for x in pr]
+        num = wf * sum(ph[p] * vsum[p] for p in range(2))
+        den = wb * 16 + wf * sum(pr[p] * 128 for p in range(2))
+        global_max[j] = num / den
+    return per_page, global_max
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 448.0])
+def test_two_level_pages_use_each_pages_own_max(tau):
+    """Reading A7, the probability quantizer's reference maximum, pinned by a
+    closed form that separates it from a maximum over several pages.  With each
+    page's own maximum every token of both pages has P = 1 and u = 8, so
+    Phat = 1.03125 (amax6: 8/6 -> E4M3 1.375, 8 * (1/1.375) -> code 6,
+    6 * 1.375 / 8) or exactly 1.0 (amax2, tau > 8), whatever the levels.  With
+    the maximum over both pages the lower page's u = 8 exp(-Delta) is quantized
+    instead (and switches to amax2 where u < tau <= 8), which this case must
+    tell apart."""
+    cfg, c = two_level_case()
+    out = run_oracle(cfg, c, tau=tau)[0]
+    per_page, global_max = two_level_closed_forms(c, tau)
+    assert np.max(np.abs(out - per_page)) < 1e-12
+    # the case discriminates: the other reading misses by at least five times
+    # the GPU parity tolerance (max-abs 2e-3) on some head
+    assert np.max(np.abs(global_max - per_page)) > 1e-2
