@@ -21,15 +21,19 @@
  *
  * Conventions shared by every call:
  *  - Every call returns an int status (BD_OK or a negative BD_ERR_*); no C++
- *    exception crosses this boundary.  Argument errors are detected on the
- *    host before anything is launched and leave device memory untouched.
+ *    exception crosses this boundary.  Argument errors in host-side values
+ *    are detected before anything is launched and leave device memory
+ *    untouched.  Device-resident indexes (block tables, destination pages,
+ *    sequence lengths) are checked by the kernels themselves: an entry out of
+ *    range is skipped, never dereferenced, and recorded in the device error
+ *    word.
  *  - All tensors are caller-owned device memory unless a parameter says
  *    "host".  The library owns only the bd_ctx, its per-layer key-shift copy
  *    and its device error word.
  *  - Launch calls take a cudaStream_t as void*, are asynchronous and never
- *    synchronize.  Device-side failures (a bounded wait that ran out) are
- *    recorded in the context's device error word; read it with
- *    bd_read_device_error().
+ *    synchronize.  Device-side failures (a bounded wait that ran out, an
+ *    out-of-range device-resident index) are recorded in the context's device
+ *    error word; read it with bd_read_device_error().
  *  - bf16 tensors are raw 16-bit bfloat16 bit patterns (const void*).
  *  - The first launch call on a device allocates the context's device state
  *    (key-shift table, error word) with cudaMalloc; make that first call, or
@@ -114,6 +118,11 @@ typedef struct bd_config {
     int query_terms;   /* 2 = dual residual query (Q ~ Q1 + Q2), 1 = single term */
     int p_mode;        /* BD_P_* */
     int p_c;           /* 1 or 8 ([cfg] probability_environment: "supports c=1 or c=8") */
+    int pool_pages;    /* physical pages in each layer's pool, or 0 = not declared.  Kernels never
+                          touch a pool page outside [0, pool_pages) (with 0: outside [0, 2^31)):
+                          a block-table or destination entry there is skipped and
+                          BD_ERR_INVALID_ARG is recorded in the device error word.  Negative
+                          entries are always skipped this way. */
 } bd_config;
 
 typedef struct bd_ctx bd_ctx;
@@ -150,6 +159,9 @@ size_t bd_query_packed_bytes(const bd_ctx* ctx);
  * one launch:
  *   k, v      : bf16 [n][128 tokens][num_kv_heads][128], device, read only.
  *   dst_pages : int32 [n], device: physical page of each input page in kv_pool.
+ *               An entry outside [0, pool_pages) (negative, with pool_pages 0)
+ *               is skipped and BD_ERR_INVALID_ARG is recorded in the device
+ *               error word.
  *   K = rotate(bf16 - mu[layer]) (per config), then per 16-element block the
  *   {4,6} search (or amax6) with per-tensor scale k_gscale; NVFP4 V uses
  *   amax6 with v_gscale; MXFP4 uses the mxfp4 search for both and ignores the
@@ -175,7 +187,8 @@ int bd_quantize_query(bd_ctx* ctx, int layer, const void* q, int B, void* q_pack
  *   k_new, v_new : bf16 [B][num_kv_heads][128], device: the new token.
  *   seq_lens     : int32 [B], device: each sequence's length L BEFORE this
  *                  token; the token takes position L.  Not modified: advance
- *                  it by one before the next decode reads the token.
+ *                  it by one before the next decode reads the token.  A
+ *                  negative L stores nothing and records BD_ERR_INVALID_ARG.
  *   sink_k/v     : bf16 [B][16][num_kv_heads][128], device, updated in place
  *                  (the token goes to row L when L < 16).
  *   tail_k/v     : bf16 [B][128][num_kv_heads][128], device, updated in place
@@ -184,7 +197,8 @@ int bd_quantize_query(bd_ctx* ctx, int layer, const void* q, int B, void* q_pack
  *                  tail page p = (L-16) div 128 (its row is 127), the page's
  *                  128 tokens are quantized into pool page block_table[b][p]
  *                  exactly as bd_quantize_kv_pages would; a page whose slot
- *                  lies beyond max_blocks is skipped and BD_ERR_INVALID_ARG is
+ *                  lies beyond max_blocks, or whose entry lies outside
+ *                  [0, pool_pages), is skipped and BD_ERR_INVALID_ARG is
  *                  recorded in the device error word.
  *   k/v_gscale, kv_pool : as bd_quantize_kv_pages.
  * This kernel does not allow the next grid to launch early, so a following
@@ -204,9 +218,15 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *                 BF16 sink and tail tokens).
  *   kv_pool     : the layer's pool (layout above), device.
  *   block_table : int32 [B][max_blocks], device: physical page of each FP4
- *                 page of each sequence.
+ *                 page of each sequence.  A page whose entry lies outside
+ *                 [0, pool_pages) (negative, with pool_pages 0) is left out of
+ *                 the attention, nothing is read for it, and BD_ERR_INVALID_ARG
+ *                 is recorded in the device error word.
  *   seq_lens    : int32 [B], device: context length L of each sequence
  *                 (0 <= L <= 16 + 128*max_blocks + 127); L = 0 gives zeros.
+ *                 A negative L is taken as 0 and a longer one keeps only its
+ *                 first max_blocks FP4 pages (and its tail rows); both record
+ *                 BD_ERR_INVALID_ARG in the device error word.
  *   sink_k/v    : bf16 [B][16][num_kv_heads][128]: tokens 0..min(L,16)-1.
  *   tail_k/v    : bf16 [B][128][num_kv_heads][128]: the partial page, tokens
  *                 16 + 128*npages ... L-1 in rows 0.., npages = max(0,L-16) div 128.
@@ -222,9 +242,9 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  * Two kernels are launched on `stream`: the split decode, then the split
  * combine, which starts under programmatic dependent launch and reads the
  * partials once the decode grid has completed.
- * Ordering: the kernel may start reading kv_pool and block_table while the
- * preceding grid in the stream, if it allows programmatic early launch,
- * still runs (this library's query, decode and combine kernels do); those
+ * Ordering: the kernel may start reading kv_pool, block_table and seq_lens
+ * while the preceding grid in the stream, if it allows programmatic early
+ * launch, still runs (this library's query, decode and combine kernels do); those
  * inputs must be written by work that completes before that grid starts
  * (bd_quantize_kv_pages and bd_append_kv never allow early launch).  q_packed, q, the sink and
  * tail rows, out and ws are touched only after the preceding grid has
@@ -256,6 +276,8 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
  *    by the caller.
  *  - The first call on a device looks up the array's device address; make
  *    that first call before capturing a stream into a CUDA graph.
+ *  - Like every launch call it must run on the context's device (the device
+ *    of the context's first launch), else it returns BD_ERR_INVALID_ARG.
  *  - No cudaMalloc, cudaFree or allocating library routine is called.  A
  *    bounded device wait that runs out is recorded in the context's error
  *    word only if that word already exists (any other launch call or
@@ -267,7 +289,8 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
                                 float k_gscale, float v_gscale, float* out, void* stream);
 
 /* Synchronize `stream`, copy the context's device error word into *out
- * (BD_OK or BD_ERR_TIMEOUT) and reset it to BD_OK. */
+ * (BD_OK, BD_ERR_TIMEOUT or BD_ERR_INVALID_ARG: the first error a kernel
+ * recorded since the last read) and reset it to BD_OK. */
 int bd_read_device_error(bd_ctx* ctx, void* stream, int* out);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an

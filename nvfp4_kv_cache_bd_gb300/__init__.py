@@ -32,14 +32,14 @@ class BDError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_layers", "num_q_heads", "num_kv_heads", "head_dim", "page_size", "sink_tokens", "format",
-        "key_search", "rotation", "centering", "query_terms", "p_mode", "p_c")]
+        "key_search", "rotation", "centering", "query_terms", "p_mode", "p_c", "pool_pages")]
 
 
 def make_config(num_layers=1, num_q_heads=32, num_kv_heads=8, format=FORMAT_NVFP4, key_search=1, rotation=1,
                 centering=1, query_terms=2, p_mode=P_AMAX2_OR_AMAX6, p_c=8, head_dim=128, page_size=128,
-                sink_tokens=16) -> Config:
+                sink_tokens=16, pool_pages=0) -> Config:
     return Config(num_layers, num_q_heads, num_kv_heads, head_dim, page_size, sink_tokens, format, key_search,
-                  rotation, centering, query_terms, p_mode, p_c)
+                  rotation, centering, query_terms, p_mode, p_c, pool_pages)
 
 
 EXPORTS = ("bd_create", "bd_destroy", "bd_status_string", "bd_set_key_shift", "bd_record_bytes",

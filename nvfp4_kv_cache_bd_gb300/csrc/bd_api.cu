@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/bd.h: argument validation,
-// context state and kernel launches.  Every argument error is detected here,
-// before any CUDA call, and returned as a status code.
+// context state and kernel launches.  Every error in a host-side argument is
+// detected here, before any CUDA call, and returned as a status code;
+// device-resident indexes are checked by the kernels (device error word).
 #include <math.h>
 #include <string.h>
 
@@ -34,6 +35,7 @@ int check_cfg(const bd_config* c) {
     if (c->p_mode < BD_P_NONE || c->p_mode > BD_P_AMAX2_OR_AMAX6) return BD_ERR_INVALID_ARG;
     // the probability kernel supports c = 1 or c = 8 (config.py probability_environment)
     if (c->p_c != 1 && c->p_c != 8) return BD_ERR_INVALID_ARG;
+    if (c->pool_pages < 0) return BD_ERR_INVALID_ARG;
     if (c->head_dim != 128 || c->page_size != 128 || c->sink_tokens != 16) return BD_ERR_UNSUPPORTED;
     if (c->num_q_heads != bd::kGroup * c->num_kv_heads || c->num_kv_heads > 16) return BD_ERR_UNSUPPORTED;
     return BD_OK;
@@ -138,8 +140,10 @@ int bd_quantize_kv_pages(bd_ctx* ctx, int layer, const void* k, const void* v, c
     a.key_search = ctx->cfg.key_search;
     a.rotation = ctx->cfg.rotation;
     a.centering = ctx->cfg.centering;
+    a.pool_pages = ctx->cfg.pool_pages;
     a.gk = k_gscale;
     a.gv = v_gscale;
+    a.err = ctx->d_err;
     return cuda_status(bd::launch_writer(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -169,6 +173,7 @@ int bd_append_kv(bd_ctx* ctx, int layer, const void* k_new, const void* v_new, c
     a.key_search = ctx->cfg.key_search;
     a.rotation = ctx->cfg.rotation;
     a.centering = ctx->cfg.centering;
+    a.pool_pages = ctx->cfg.pool_pages;
     a.gk = k_gscale;
     a.gv = v_gscale;
     a.seq_lens = seq_lens;
@@ -249,6 +254,7 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     a.hkv = ctx->cfg.num_kv_heads;
     a.max_blocks = max_blocks;
     bd::decode_splits(B, a.hkv, max_blocks, &a.nsplit, &a.pages_per_split);
+    a.pool_pages = ctx->cfg.pool_pages;
     a.format = ctx->cfg.format;
     a.centering = ctx->cfg.centering;
     a.p_mode = ctx->cfg.p_mode;
@@ -278,6 +284,14 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     // the fixed scratch must hold this call's split partials
     const size_t need = bd_decode_workspace_size(ctx, B, max_blocks);
     if (need > bd::kNoAllocScratchBytes) return BD_ERR_WORKSPACE;
+    {
+        // a context is bound to the device of its first launch: its error word
+        // lives there
+        std::lock_guard<std::mutex> g(ctx->mu_lock);
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+        if (ctx->d_mu && dev != ctx->device) return BD_ERR_INVALID_ARG;
+    }
     void* scratch = nullptr;
     if (bd::noalloc_scratch(&scratch) != cudaSuccess) return BD_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -302,6 +316,7 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     a.hkv = ctx->cfg.num_kv_heads;
     a.max_blocks = max_blocks;
     bd::decode_splits(B, a.hkv, max_blocks, &a.nsplit, &a.pages_per_split);
+    a.pool_pages = ctx->cfg.pool_pages;
     a.format = ctx->cfg.format;
     a.centering = ctx->cfg.centering;
     a.p_mode = ctx->cfg.p_mode;

@@ -78,6 +78,7 @@ struct alignas(16) Ctl {
     int abort_flag;
     int next_page;             // next page index a consumer warp takes
     int tagK[kNK], tagV[kNV];  // page index each slot's latest fill holds (-1: none)
+    int badK[kNK];             // 1: that fill's block-table entry was out of range (no data, skip the page)
 };
 constexpr int kPTabBytes = 2 * 128 * 4;                        // scale tables (see decode_kernel)
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kPTabBytes;
@@ -195,7 +196,7 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
     const int tid = threadIdx.x;
     // the sink/tail rows and q may be produced by the preceding grid
     griddep_wait();
-    if (T == 0) {
+    if (T <= 0) {
         if (tid < 4) {
             ctl->wm[kConsumers][tid] = -INFINITY;
             ctl->wl[kConsumers][tid] = 0.0f;
@@ -391,6 +392,20 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
             if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
             ctl->abort_flag = 1;
             break;
+        }
+        if (ctl->badK[sk]) {
+            // out-of-range block-table entry: nothing was copied for this page
+            // and it is left out; hand both slots back in ring order
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyK[sk]));
+            if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
+                if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+                ctl->abort_flag = 1;
+                break;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyV[sv]));
+            continue;
         }
         const uint8_t* Ks = smem + sk * kMaxRec;
         const uint8_t* Vs = smem + (kNK + sv) * kMaxRec;
@@ -754,7 +769,13 @@ template <int FMT, int PM>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {   // 128 registers
     extern __shared__ __align__(128) uint8_t smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int L = a.seq_lens[b];
+    // a negative length counts as 0; one past the block table's capacity keeps
+    // its first max_blocks pages; both are argument errors
+    const int Lraw = a.seq_lens[b];
+    const int L = max(0, Lraw);
+    if (split == 0 && h == 0 && threadIdx.x == 0 &&
+        (Lraw < 0 || (int64_t)Lraw > kSink + (int64_t)kPage * a.max_blocks + (kPage - 1)))
+        record_error(a.err, BD_ERR_INVALID_ARG);
     float* part = a.parts + ((size_t)(b * a.hq + 4 * h) * (a.nsplit + 1) + split) * kPartStride;
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + kRingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -793,6 +814,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                 mbar_init(smem_u32(&ctl->fullK[s]), 1);
                 mbar_init(smem_u32(&ctl->emptyK[s]), 1);
                 ctl->tagK[s] = -1;
+                ctl->badK[s] = 0;
             }
             for (int s = 0; s < kNV; ++s) {
                 mbar_init(smem_u32(&ctl->fullV[s]), 1);
@@ -840,13 +862,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                         break;
                     }
                     const int64_t phys = bt[k];
-                    const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
+                    const bool ok = page_ok(phys, a.pool_pages);
                     const uint32_t full = smem_u32(&fullb[s]);
+                    if (isK) ctl->badK[s] = ok ? 0 : 1;   // published by the tag's release
                     // tag the fill before it is armed: consumers accept a completed
                     // phase only together with their own page index
                     st_release_shared(&tag[s], k);
-                    mbar_arrive_expect_tx(full, RB);
-                    bulk_g2s_hint(smem_u32(slots + s * kMaxRec), rec, RB, full, policy);
+                    if (ok) {
+                        const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
+                        mbar_arrive_expect_tx(full, RB);
+                        bulk_g2s_hint(smem_u32(slots + s * kMaxRec), rec, RB, full, policy);
+                    } else {
+                        // an entry outside the pool: complete the phase without data
+                        if (isK) record_error(a.err, BD_ERR_INVALID_ARG);
+                        mbar_arrive(full);
+                    }
                 }
             }
             __syncthreads();   // (A)
@@ -889,14 +919,38 @@ __global__ void bounded_wait_kernel(int* err, uint64_t limit_ns) {
 
 }  // namespace
 
+namespace {
+
+// Host state of the decode launcher per device, filled on first use under one
+// lock: the SM count and which decode instances have their dynamic
+// shared-memory limit raised (a per-device function attribute).
+struct DeviceState {
+    int sms = 0;
+    bool smem_attr[2][3] = {};
+};
+std::mutex g_dev_lock;
+DeviceState g_dev[kMaxDevices];
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int device_sms() {
+    const int dev = current_device();
+    if (dev < 0) return 148;
+    std::lock_guard<std::mutex> g(g_dev_lock);
+    int& sms = g_dev[dev].sms;
+    if (sms <= 0 && (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0))
+        sms = 148;
+    return sms;
+}
+
+}  // namespace
+
 void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-            sms = 148;
-    }
+    const int sms = device_sms();
     // two CTAs fit per SM; split 0 of every (sequence, kv head) is the BF16
     // sink/tail CTA, so a single wave holds units * (splits + 1) CTAs
     const int slots = 2 * sms;
@@ -933,13 +987,17 @@ DecodeFn pick_decode(int p_mode) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.B == 0) return cudaSuccess;
-    static bool attr_set[2][3] = {};
     const int f = a.format, pm = a.p_mode;
     DecodeFn kern = (f == BD_FORMAT_NVFP4) ? pick_decode<BD_FORMAT_NVFP4>(pm) : pick_decode<BD_FORMAT_MXFP4>(pm);
-    if (!attr_set[f][pm]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set[f][pm] = true;
+    {
+        const int dev = current_device();
+        if (dev < 0) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> g(g_dev_lock);
+        if (!g_dev[dev].smem_attr[f][pm]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            g_dev[dev].smem_attr[f][pm] = true;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.nsplit + 1), (unsigned)a.hkv, (unsigned)a.B);
@@ -976,11 +1034,11 @@ cudaError_t noalloc_scratch(void** out) {
     // memory: the device address is looked up once per device, with that
     // device current, and cached.
     static std::mutex lock;
-    static void* addr[kMaxNoAllocDevices] = {};
+    static void* addr[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxNoAllocDevices) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> g(lock);
     if (!addr[dev]) {
         void* p = nullptr;

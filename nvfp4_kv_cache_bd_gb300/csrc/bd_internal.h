@@ -16,6 +16,7 @@ constexpr int kGroup = 4;        // query heads per kv head
 constexpr int kCodeBytes = 8192; // codes of one record
 constexpr int kPartStride = 132; // floats per split partial: m, l, pad, pad, O[128]
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded waits give up after 1 s
+constexpr int kMaxDevices = 64;  // per-device host caches (attributes, SM counts, scratch addresses)
 
 __host__ __device__ inline int nblocks(int format) { return format == BD_FORMAT_NVFP4 ? 8 : 4; }
 __host__ __device__ inline int record_bytes(int format) { return kCodeBytes + kPage * nblocks(format); }
@@ -28,6 +29,7 @@ struct WriterArgs {
     const float* mu;          // [Hkv][128] of this layer (device)
     uint8_t* pool;
     int n, hkv, format, key_search, rotation, centering;
+    int pool_pages;           // 0: only negative destination pages are rejected
     float gk, gv;
     // Append mode (bd_append_kv) when seq_lens is set: n = B sequences, k/v
     // are the BF16 tail buffers [B][128][Hkv][128]; the new token is stored
@@ -68,6 +70,7 @@ struct DecodeArgs {
     int* err;
     size_t qstride;
     int B, hq, hkv, max_blocks, nsplit, pages_per_split;
+    int pool_pages;           // 0: only negative block-table entries are rejected
     int format, centering, p_mode, p_c;
     float tau, gk, gv;
 };
@@ -81,7 +84,12 @@ size_t decode_ws_bytes(int B, int hq, int nsplit);
 
 // Fixed device scratch of bd_decode_attention_noalloc (see bd_decode.cu).
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
-constexpr int kMaxNoAllocDevices = 64;
 cudaError_t noalloc_scratch(void** out);
+
+// A pool page index the kernels may dereference: in [0, pool_pages), or any
+// non-negative int when the pool size is not declared.
+__host__ __device__ inline bool page_ok(int64_t phys, int pool_pages) {
+    return phys >= 0 && (pool_pages <= 0 || phys < pool_pages);
+}
 
 }  // namespace bd

@@ -338,9 +338,14 @@ __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) w
     const size_t tok_stride = (size_t)a.hkv * kD;
     int64_t page;
     const uint16_t* newrow = nullptr;   // append mode: the new token's row, staged as the page's last row
+    const bool reporter = threadIdx.x == 0 && kv == 0 && blockIdx.z == 0;   // one report per page
     if (a.seq_lens) {
         // append the token at position L (pg is the sequence) ...
         const int L = a.seq_lens[pg];
+        if (L < 0) {
+            if (reporter && h == 0) record_error(a.err, BD_ERR_INVALID_ARG);
+            return;
+        }
         const uint16_t* nrow = (kv == 0 ? a.k_new : a.v_new) + ((size_t)pg * a.hkv + h) * kD;
         if (L < kSink) {
             uint16_t* dst = (kv == 0 ? a.sink_k : a.sink_v) + (((size_t)pg * kSink + L) * a.hkv + h) * kD;
@@ -356,13 +361,17 @@ __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) w
         // ... and pack the tail page it completes
         if (r != kPage - 1) return;
         if (p >= a.max_blocks) {
-            if (threadIdx.x == 0 && kv == 0 && blockIdx.z == 0) record_error(a.err, BD_ERR_INVALID_ARG);
+            if (reporter) record_error(a.err, BD_ERR_INVALID_ARG);
             return;
         }
         page = a.block_table[(size_t)pg * a.max_blocks + p];
         newrow = nrow;
     } else {
         page = a.dst_pages[pg];
+    }
+    if (!page_ok(page, a.pool_pages)) {   // never write outside the pool
+        if (reporter) record_error(a.err, BD_ERR_INVALID_ARG);
+        return;
     }
     uint8_t* rec = a.pool + ((page * a.hkv + h) * 2 + kv) * (int64_t)record_bytes(a.format);
     const uint16_t* src = (kv == 0 ? a.k : a.v) + (((size_t)pg * kPage + row0) * a.hkv + h) * kD;

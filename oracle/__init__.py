@@ -40,13 +40,14 @@ FLAG_QUANT_DENOM = 1
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_q_heads", "num_kv_heads", "head_dim", "page_size", "sink_tokens", "format",
-        "key_search", "rotation", "centering", "query_terms", "p_mode", "p_c")]
+        "key_search", "rotation", "centering", "query_terms", "p_mode", "p_c", "pool_pages")]
 
 
 def make_config(num_q_heads=32, num_kv_heads=8, fmt=FMT_NVFP4, key_search=1, rotation=1,
-                centering=1, query_terms=2, p_mode=P_AMAX2_OR_AMAX6, p_c=8, sink_tokens=16) -> Config:
+                centering=1, query_terms=2, p_mode=P_AMAX2_OR_AMAX6, p_c=8, sink_tokens=16,
+                pool_pages=0) -> Config:
     return Config(num_q_heads, num_kv_heads, 128, 128, sink_tokens, fmt, key_search, rotation,
-                  centering, query_terms, p_mode, p_c)
+                  centering, query_terms, p_mode, p_c, pool_pages)
 
 
 _lib = None
@@ -202,7 +203,8 @@ def mem_ratio(cfg: Config) -> float:
 
 def quantize_kv_pages(cfg: Config, k, v, dst_pages, mu, k_gscale: float, v_gscale: float,
                       pool: np.ndarray) -> np.ndarray:
-    """k, v: uint16 [n][128][Hkv][128]; writes the records into pool (uint8) in place."""
+    """k, v: uint16 [n][128][Hkv][128]; writes the records into pool (uint8) in
+    place (destinations outside the pool are skipped)."""
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     dst = _c(dst_pages, np.int32)

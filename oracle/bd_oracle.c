@@ -34,12 +34,13 @@
  *
  * Pins: the CPU tests check every function here against something other than
  * itself -- brute force over the code tables, closed forms, the explicit
- * Sylvester matrix, textbook softmax attention in fp64 -- except the
- * probability quantizer's reading of the pages (per-page reference maximum,
- * amax2-or-amax6 by tau on u = c*P, the unquantized denominator).  That part
- * is pinned only by its endpoints (tau = 0, tau = 448) and closed forms (all
- * keys equal); beyond them its parity is unpinned, since the pages print no
- * value to check it against.
+ * Sylvester matrix, textbook softmax attention in fp64.  The probability
+ * quantizer's reading of the pages (each page's own reference maximum,
+ * amax2-or-amax6 by tau on u = c*P, the unquantized denominator) is pinned by
+ * its endpoints (tau = 0, tau = 448) and by closed forms: all keys equal, and
+ * two pages whose keys are constant at two levels, which tells a per-page
+ * maximum from one taken over several pages.  No value printed by the pages
+ * pins it further: they print none.
  */
 #include <math.h>
 #include <stdint.h>
@@ -63,7 +64,16 @@ typedef struct {
     int query_terms;  /* 1 or 2 */
     int p_mode;       /* 0 = exact P (no quantization), 1 = amax6, 2 = amax2-or-amax6 */
     int p_c;          /* 1 or 8 */
+    int pool_pages;   /* physical pages of a layer's pool; 0 = not declared */
 } or_config;
+
+/* A physical page the path may touch: in [0, pool_pages), or any
+ * non-negative index when the pool size is not declared.  The library's
+ * definition of an out-of-range block-table or destination entry: it is left
+ * out (no record read or written). */
+static int page_in_pool(const or_config* c, int64_t phys) {
+    return phys >= 0 && (c->pool_pages <= 0 || phys < c->pool_pages);
+}
 
 /* attention debug flags */
 #define OR_FLAG_QUANT_DENOM 1  /* softmax denominator = sum of quantized P instead of exact P */
@@ -380,14 +390,20 @@ static void quantize_vec(const or_config* c, const float* y, int is_key, float g
  * k, v: n pages of [128 tokens][Hkv][128] bf16.  dst_pages[n]: physical page
  * of each.  mu: [Hkv][128] key mean of this layer (NULL = zero).
  * K: x = bf16 - mu (centering), rotated (rotation), then {4,6} / amax6 / MX.
- * V: amax6 (NVFP4) or MX search, no centering, no rotation. */
+ * V: amax6 (NVFP4) or MX search, no centering, no rotation.
+ * A destination outside the pool is skipped; returns the number skipped. */
 int or_quantize_kv_pages(const or_config* c, const uint16_t* k, const uint16_t* v,
                          const int32_t* dst_pages, int n, const float* mu,
                          float k_gscale, float v_gscale, uint8_t* pool) {
     int H = c->num_kv_heads;
     float x[OR_D];
     uint8_t codes[OR_D], sbs[8];
+    int skipped = 0;
     for (int pg = 0; pg < n; pg++) {
+        if (!page_in_pool(c, dst_pages[pg])) {
+            skipped++;
+            continue;
+        }
         for (int h = 0; h < H; h++) {
             uint8_t* krec = pool + rec_off(c, dst_pages[pg], h, 0);
             uint8_t* vrec = pool + rec_off(c, dst_pages[pg], h, 1);
@@ -407,7 +423,7 @@ int or_quantize_kv_pages(const or_config* c, const uint16_t* k, const uint16_t* 
             }
         }
     }
-    return 0;
+    return skipped;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -634,7 +650,10 @@ static void merge(const seg_t* segs, int n, double* o) {
  * length L: sink = tokens [0, min(L,16)); FP4 pages p = 0..npages-1 with
  * npages = max(0, L-16) div 128 holding tokens 16+128p ..; tail = the
  * remaining max(0, L-16) - 128 npages tokens.  Query head j reads KV head
- * j div (Hq/Hkv); softmax scale 1/sqrt(128).
+ * j div (Hq/Hkv); softmax scale 1/sqrt(128).  Out-of-range arguments, as the
+ * library defines them: a negative L counts as 0; only the first max_blocks
+ * pages exist; a page whose block-table entry lies outside the pool is left
+ * out of the attention.
  * out: [B][Hq][128] fp64. */
 int or_decode_attention(const or_config* c, const uint8_t* q_packed, const uint16_t* q, const float* mu,
                         const uint8_t* pool, const int32_t* block_table, int max_blocks,
@@ -647,11 +666,12 @@ int or_decode_attention(const or_config* c, const uint8_t* q_packed, const uint1
     int64_t stride = or_qpack_stride(c);
     double qh[OR_D];
     for (int b = 0; b < B; b++) {
-        int L = seq_lens[b];
+        int L = seq_lens[b] > 0 ? seq_lens[b] : 0;
         int nsink = L < SINK ? L : SINK;
         int rest = L - SINK > 0 ? L - SINK : 0;
         int npages = rest / OR_PAGE;
         int ntail = rest - npages * OR_PAGE;
+        if (npages > max_blocks) npages = max_blocks;
         seg_t* segs = (seg_t*)malloc(sizeof(seg_t) * (size_t)(npages + 2));
         const uint8_t* qp = q_packed + b * stride;
         for (int j = 0; j < Hq; j++) {
@@ -667,6 +687,10 @@ int or_decode_attention(const or_config* c, const uint8_t* q_packed, const uint1
                          ntail, H, h, sm, &segs[1]);
             for (int p = 0; p < npages; p++) {
                 int64_t phys = block_table[(int64_t)b * max_blocks + p];
+                if (!page_in_pool(c, phys)) {
+                    seg_init(&segs[2 + p]);   /* empty: left out of the merge */
+                    continue;
+                }
                 fp4_page_segment(c, pool + rec_off(c, phys, h, 0), pool + rec_off(c, phys, h, 1), qh, qmu, sm,
                                  tau, gk, gv, flags, &segs[2 + p]);
             }

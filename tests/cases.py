@@ -30,6 +30,7 @@ class Spec:
     tau: float = 1.0
     shuffle: bool = True
     spare_pages: int = 2
+    pool_pages: int = 0    # declared pool size (0: not declared)
 
 
 class Case:
@@ -89,10 +90,11 @@ def build(spec: Spec, ctx=None) -> Case:
         c.gv = 1.0
     c.nphys = nphys
     c.ocfg = oracle.make_config(fmt=spec.fmt, key_search=spec.key_search, rotation=spec.rotation,
-                                centering=spec.centering, query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c)
+                                centering=spec.centering, query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c,
+                                pool_pages=spec.pool_pages)
     c.ctx = ctx if ctx is not None else bd.Context(bd.make_config(
         format=spec.fmt, key_search=spec.key_search, rotation=spec.rotation, centering=spec.centering,
-        query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c))
+        query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c, pool_pages=spec.pool_pages))
     c.rec = oracle.record_bytes(c.ocfg)
     c.qstride = oracle.qpack_stride(c.ocfg)
     return c

@@ -57,6 +57,7 @@ def cfg(**kw):
     (dict(format=2), bd.ERR_INVALID_ARG),
     (dict(rotation=2), bd.ERR_INVALID_ARG),
     (dict(num_layers=0), bd.ERR_INVALID_ARG),
+    (dict(pool_pages=-1), bd.ERR_INVALID_ARG),
     (dict(head_dim=64), bd.ERR_UNSUPPORTED),
     (dict(page_size=16), bd.ERR_UNSUPPORTED),
     (dict(sink_tokens=4), bd.ERR_UNSUPPORTED),

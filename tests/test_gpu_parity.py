@@ -251,3 +251,80 @@ def test_two_level_pages_use_each_pages_own_max(tau):
     mx, rl = cases.attn_errors(gpu["out"], ora["out"])
     assert mx < MAX_ABS and rl < REL_L2, (mx, rl)
     assert bd.read_device_error(c.ctx) == bd.OK
+
+
+def test_out_of_range_pages_are_skipped_and_reported():
+    """Device-resident indexes outside the declared pool (bd_config.pool_pages)
+    are never dereferenced: the writer skips such a destination, the decode
+    leaves such a page out, and both record BD_ERR_INVALID_ARG.  The pool
+    handed to the library sits two pages into a larger allocation, so pages
+    -2, -1, n and n + 1 are still inside it and nothing could fault even if a
+    check were missing; the bytes there must keep their fill value."""
+    n = 5
+    spec = cases.Spec(lens=[16 + 128 * n + 40, 16 + 128 * 2 + 9], seed=93, shuffle=False, spare_pages=0)
+    c0 = cases.build(spec)
+    npages = c0.nphys
+    spec.pool_pages = npages
+    c = cases.build(spec)
+    dev = "cuda"
+    H, rec = 8, c.rec
+    page_bytes = H * 2 * rec
+    big = torch.full(((npages + 4) * page_bytes,), cases.FILL, dtype=torch.uint8, device=dev)
+    pool = big[2 * page_bytes:(npages + 2) * page_bytes]
+    bd.set_key_shift(c.ctx, 0, c.mu)
+    kp = torch.cat([c.k_pages, c.k_pages[:1]]).to(dev)
+    vp = torch.cat([c.v_pages, c.v_pages[:1]]).to(dev)
+    dst = torch.from_numpy(np.concatenate([c.dst, [npages]]).astype(np.int32)).to(dev)
+    bd.quantize_kv_pages(c.ctx, 0, kp, vp, dst, c.gk, c.gv, pool)
+    torch.cuda.synchronize()
+    assert bd.read_device_error(c.ctx) == bd.ERR_INVALID_ARG
+    ora = cases.run_oracle(c, pool_only=True)
+    assert np.array_equal(pool.cpu().numpy(), ora["pool"])
+    outside = torch.cat([big[:2 * page_bytes], big[(npages + 2) * page_bytes:]])
+    assert bool((outside == cases.FILL).all())
+    # decode with entries n (one past the pool) and -1 in the block table
+    c.block_table[0, 1] = npages
+    c.block_table[0, 3] = -1
+    c.block_table[1, 0] = npages + 1
+    B = len(spec.lens)
+    q = c.q.to(dev)
+    qp = torch.zeros(B, c.qstride, dtype=torch.uint8, device=dev)
+    bd.quantize_query(c.ctx, 0, q, qp)
+    bt = torch.from_numpy(c.block_table).to(dev)
+    sl = torch.from_numpy(c.seq_lens).to(dev)
+    args = [x.to(dev) for x in (c.sink_k, c.sink_v, c.tail_k, c.tail_v)]
+    out = torch.full((B, 32, 128), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.zeros(bd.decode_workspace_size(c.ctx, B, bt.shape[1]) // 4 + 1, dtype=torch.float32, device=dev)
+    bd.decode_attention(c.ctx, 0, qp, q, pool, bt, sl, *args, c.spec.tau, c.gk, c.gv, out, ws)
+    torch.cuda.synchronize()
+    assert bd.read_device_error(c.ctx) == bd.ERR_INVALID_ARG
+    ref = cases.run_oracle(c)["out"]
+    mx, rl = cases.attn_errors(out.cpu().double().numpy(), ref)
+    assert mx < MAX_ABS and rl < REL_L2, (mx, rl)
+
+
+def test_negative_and_overlong_lengths():
+    """A negative length counts as 0 (zero output) and a length past the
+    block table's capacity keeps its first max_blocks pages; both are
+    reported in the device error word."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 3 + 50, 16 + 128 * 3 + 50], seed=94))
+    gpu = cases.run_gpu(c)
+    assert bd.read_device_error(c.ctx) == bd.OK
+    dev = "cuda"
+    B = 2
+    sl = torch.tensor([-3, 16 + 128 * 7 + 50], dtype=torch.int32, device=dev)   # capacity: 3 pages + 127
+    out = torch.full((B, 32, 128), float("nan"), dtype=torch.float32, device=dev)
+    bt = torch.from_numpy(c.block_table).to(dev)
+    ws = torch.zeros(bd.decode_workspace_size(c.ctx, B, bt.shape[1]) // 4 + 1, dtype=torch.float32, device=dev)
+    bd.decode_attention(c.ctx, 0, torch.from_numpy(gpu["qp"]).to(dev), c.q.to(dev),
+                        torch.from_numpy(gpu["pool"]).to(dev), bt, sl,
+                        *[x.to(dev) for x in (c.sink_k, c.sink_v, c.tail_k, c.tail_v)], c.spec.tau, c.gk, c.gv,
+                        out, ws)
+    torch.cuda.synchronize()
+    assert bd.read_device_error(c.ctx) == bd.ERR_INVALID_ARG
+    c.seq_lens = sl.cpu().numpy()
+    ref = cases.run_oracle(c)["out"]
+    o = out.cpu().double().numpy()
+    assert not o[0].any()
+    mx, rl = cases.attn_errors(o, ref)
+    assert mx < MAX_ABS and rl < REL_L2, (mx, rl)

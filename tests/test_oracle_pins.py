@@ -742,3 +742,62 @@ def test_two_level_pages_use_each_pages_own_max(tau):
     # the case discriminates: the other reading misses by at least five times
     # the GPU parity tolerance (max-abs 2e-3) on some head
     assert np.max(np.abs(global_max - per_page)) > 1e-2
+
+
+def test_out_of_range_pages_and_lengths():
+    """The library's definition of out-of-range device-resident arguments,
+    checked on the oracle with exact probabilities (one softmax over the
+    dequantized operands, as above): a page whose block-table entry lies
+    outside [0, pool_pages) is left out, a negative length counts as 0, and a
+    sequence longer than its block table keeps its first max_blocks pages."""
+    n = 4
+    cfg = oracle.make_config(p_mode=oracle.P_NONE, pool_pages=n)
+    L = 16 + n * 128 + 20
+    c = build_case(L, 33, cfg, shuffle=False)
+    sm = 1 / np.sqrt(128)
+    qhat = layout.query_record(0, 32, c["qp"][0])[0]
+    q, k, v = (c[x][0].double().numpy() for x in ("q", "k", "v"))
+
+    def softmax_ref(pages, tail):
+        out = np.zeros((32, 128))
+        for j in range(32):
+            h = j // 4
+            lg = [sm * q[j] @ k[t, h] for t in range(16)]
+            vals = [v[t, h] for t in range(16)]
+            for p in pages:
+                kv = layout.k_record(0, layout.pool_record(c["pool"], 0, 8, c["bt"][0, p], h, 0))[2]
+                vv = layout.v_record(0, layout.pool_record(c["pool"], 0, 8, c["bt"][0, p], h, 1))[2]
+                lg += list(sm * (kv @ qhat[j] * c["gk"] + q[j] @ c["mu"][h].double().numpy()))
+                vals += list(vv * c["gv"])
+            for t in tail:
+                lg.append(sm * q[j] @ k[t, h])
+                vals.append(v[t, h])
+            lg = np.array(lg)
+            w = np.exp(lg - lg.max())
+            out[j] = (w[:, None] * np.array(vals)).sum(0) / w.sum()
+        return out
+
+    tail = range(16 + n * 128, L)
+    good = run_oracle(cfg, c)[0]
+    assert np.max(np.abs(good - softmax_ref(range(n), tail))) < 1e-12
+    bt = c["bt"].copy()
+    c["bt"] = bt.copy()
+    c["bt"][0, 1] = n            # one past the declared pool
+    c["bt"][0, 3] = -7           # negative
+    out = run_oracle(cfg, c)[0]
+    c["bt"] = bt
+    assert np.max(np.abs(out - softmax_ref([0, 2], tail))) < 1e-12
+    # a sequence longer than its block table (max_blocks = 2): pages 0 and 1
+    # only, and the same tail rows
+    c2 = dict(c, bt=bt[:, :2].copy())
+    assert np.max(np.abs(run_oracle(cfg, c2)[0] - softmax_ref([0, 1], tail))) < 1e-12
+    c3 = dict(c, seq_lens=np.array([-5], np.int32))
+    assert not run_oracle(cfg, c3).any()
+    # the writer skips a destination outside the pool and reports it
+    pool = c["pool"].copy()
+    kp = c["k"][0][16:16 + 128].reshape(1, 128, 8, 128).view(torch.uint16).numpy()
+    vp = c["v"][0][16:16 + 128].reshape(1, 128, 8, 128).view(torch.uint16).numpy()
+    assert oracle.lib().or_quantize_kv_pages(
+        oracle.ctypes.byref(cfg), oracle._p(np.ascontiguousarray(kp)), oracle._p(np.ascontiguousarray(vp)),
+        oracle._p(np.array([n], np.int32)), 1, oracle._p(c["mu"].numpy()), c["gk"], c["gv"], oracle._p(pool)) == 1
+    assert np.array_equal(pool, c["pool"])
