@@ -1,18 +1,25 @@
 """Benchmark of the NVFP4 KV-cache hot path on one GB300 (or N replicas).
 
-Default workload (the metric's configuration): single-sequence decode at a
+Headline workload (the metric's configuration): single-sequence decode at a
 131072-token context, 36 layers, 32 query / 8 KV heads, head_dim 128, full
 recipe (16-token BF16 sink, Hadamard + centered keys with {4,6} scales,
 two-term query, FP4 probabilities with c = 8, tau = 1.0), 128-token pages
 with a shuffled physical block table.  One timed step = for each of the 36
-layers, bd_quantize_query + bd_decode_attention.  The page-fill writer, which
-runs once per 128 decode steps, is timed in the same run on its own workload
-(64 sequences x 36 layers x 8 KV heads, one freshly filled 128-token page of K
-and V each) and reported as writer tokens/s.
+layers, bd_quantize_query + bd_decode_attention, replayed as one CUDA graph.
+
+The same run also times, each on its own workload and with its own clock
+window, every other configuration of the workload table ("configs" in the
+line): the 4096-token single-layer parity case, the page-fill writer (64
+sequences x 36 layers x 8 KV heads, one freshly filled 128-token page of K and
+V each; NVFP4 and MXFP4), the 32768-token decode, the 128K tau sweep
+{0, 0.5, 4, 448} and the 32-sequence batch (log-uniform lengths in
+[1024, 65536]; NVFP4 / MXFP4 x rotation + centering on / off), plus the
+decode-token append.  --no-configs keeps only the headline.
 
 Inputs are seeded synthetic tensors (nvfp4_kv_cache_bd_gb300.synth) resident
-in HBM before timing; the 36 layers' packed pools (5.4 GB) exceed L2, so no
-explicit flush is needed.  Prints ONE JSON line on rank 0.
+in HBM before timing; every decode step streams more distinct pool bytes than
+L2 holds (asserted), so no explicit flush is needed.  Prints ONE JSON line on
+rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -45,12 +52,10 @@ def parse():
     ap.add_argument("--ctx", type=int, default=CTX)
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--tau", type=float, default=1.0)
-    ap.add_argument("--no-writer", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
+    ap.add_argument("--config-steps", type=int, default=0,
+                    help="timed steps of each other configuration (default: --steps, at most 100)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--tau-sweep", action="store_true")
-    ap.add_argument("--suite", action="store_true",
-                    help="also measure the 32K decode, the tau sweep at the default context, the 32-sequence batch "
-                         "(NVFP4 / MXFP4, recipe on / off) and the MXFP4 writer; attached as 'suite'")
     return ap.parse_args()
 
 
@@ -69,12 +74,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, interval_ms: int = 50):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
         self.interval_ms = interval_ms
         self.proc = None
         self.path = None
-        self.window = None
+        self.windows = []
 
     def start(self):
         try:
@@ -98,15 +103,15 @@ class ClockSampler:
             return 0
 
     def mark_begin(self):
-        """Called right before the timed region: rows from here on count."""
+        """Called right before a timed region: rows from here on count."""
         if self.proc is not None:
-            self.window = [self._rows(), None]
+            self.windows.append([self._rows(), None])
 
     def mark_end(self):
-        """Called right after the timed region (after its synchronize)."""
-        if self.proc is not None and self.window is not None:
+        """Called right after a timed region (after its synchronize)."""
+        if self.proc is not None and self.windows and self.windows[-1][1] is None:
             time.sleep(self.interval_ms / 1000.0)
-            self.window[1] = self._rows()
+            self.windows[-1][1] = self._rows()
 
     def stop(self):
         if self.proc is None:
@@ -118,8 +123,8 @@ class ClockSampler:
             self.proc.kill()
         lines = open(self.path).read().splitlines()
         os.unlink(self.path)
-        if self.window is not None:
-            lines = lines[self.window[0]:self.window[1]]
+        if self.windows:
+            lines = [ln for a, b in self.windows if b is not None for ln in lines[a:b]]
         rows = []
         for line in lines:
             parts = [p.strip() for p in line.split(",")]
@@ -132,7 +137,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "timed_regions": len(self.windows),
+                "interval_ms": self.interval_ms}
 
 
 # ------------------------------------------------------------- workload ----
@@ -230,6 +236,16 @@ class DecodeWorkload:
     def step(self, stream=None, evs=None):
         for l in range(self.layers):
             self.layer(l, stream, ev=None if evs is None else evs[l])
+
+    def decode_step(self, stream=None):
+        """The step without the query kernels: each layer's packed query is
+        left in place by an earlier step()."""
+        for l in range(self.layers):
+            sk, sv = self.sinks[l]
+            tk, tv = self.tails[l]
+            gk, gv = self.gscales[l]
+            self.bd.decode_attention(self.ctx, l, self.qp[l], self.qs[l], self.pools[l], self.block_table,
+                                     self.seq_lens, sk, sv, tk, tv, self.tau, gk, gv, self.out[l], self.ws, stream)
 
 
 def graphed(fn, torch):
@@ -415,6 +431,9 @@ def run_reference(args):
 
 # ----------------------------------------------------------------- native --
 
+L2_BYTES = 129 * 1024 * 1024
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -437,29 +456,37 @@ def main():
         pg = dist
     stream = torch.cuda.current_stream()
     hbm_peak, peak_src = peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    cfg_steps = args.config_steps or min(args.steps, 100)
 
     # ---------------- decode workload (headline)
     wl = DecodeWorkload(args.ctx, args.layers, args.tau, device, seed=rank)
+    step_bytes = wl.bytes_per_layer * args.layers
+    assert step_bytes > L2_BYTES, "a step must stream more than L2 holds"
     fn = graphed(lambda: wl.step(), torch)   # one step = 36 x (query quantization + decode)
-    # roofline pass: events bracket each decode call (decode kernel + split combine)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
-    clocks = ClockSampler(local)
-    clocks.start()
     ms = timed(fn, args.steps, args.warmup, stream, torch, pg, clocks)
-    clk = clocks.stop()
+    # the decode alone inside a graphed step (packed queries left by the step
+    # above): its per-layer time is the decode launch's in-step duration
+    dec_graph_ms = timed(graphed(lambda: wl.decode_step(), torch), args.steps, args.warmup, stream, torch, pg,
+                         clocks)
+    # stream-ordered, one decode call at a time with events around it
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
     durs = []
     for _ in range(10):
         wl.step(evs=evs)
         torch.cuda.synchronize()
-        durs += [a.elapsed_time(b) for a, b in evs]
+        durs += [a_.elapsed_time(b_) for a_, b_ in evs]
     err = bd.read_device_error(wl.ctx)
     if err != bd.OK:
         raise RuntimeError(f"device error word: {bd.status_string(err)}")
-    dec_ms = statistics.mean(durs)
     ms = max_over_ranks(ms, pg, device)
+    dec_graph_ms = max_over_ranks(dec_graph_ms, pg, device)
     us_step = ms * 1000.0
-    step_bytes = wl.bytes_per_layer * args.layers
-    achieved = wl.bytes_per_layer / (dec_ms * 1e-3) / 1e9
+    call_ms = statistics.mean(durs)
+    in_step_ms = dec_graph_ms / args.layers
+    achieved_in_step = wl.bytes_per_layer / (in_step_ms * 1e-3) / 1e9
+    achieved_call = wl.bytes_per_layer / (call_ms * 1e-3) / 1e9
 
     # ---------------- end to end through the C ABI with host buffers: one
     # host->device copy of the step's queries (all layers) from pinned memory,
@@ -475,26 +502,29 @@ def main():
             wl.layer(l, q=q_dev[l], out=out_dev[l])
         out_host.copy_(out_dev, non_blocking=True)
 
-    e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg)
+    e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg, clocks)
     e2e_ms = max_over_ranks(e2e_ms, pg, device)
     h2d = q_host.numel() * q_host.element_size()
     d2h = out_host.numel() * out_host.element_size()
 
-    tau_sweep = None
-    if args.tau_sweep:
-        tau_sweep = {}
+    configs = None
+    if not args.no_configs:
+        configs = {}
+        gbs = step_bytes / (ms * 1e-3) / 1e9
+        sweep = {str(args.tau): {"us_per_step": us_step, "packed_kv_gbs": gbs, "frac_of_peak": gbs / hbm_peak,
+                                 "packed_bytes_per_step": step_bytes, "note": "the headline measurement"}}
         for tau in (0.0, 0.5, 4.0, 448.0):
             wl.tau = tau
-            tau_sweep[str(tau)] = timed(graphed(lambda: wl.step(), torch), max(5, args.steps // 2), args.warmup,
-                                        stream, torch, pg) * 1000.0
+            sweep[str(tau)] = step_rate(wl, cfg_steps, args.warmup, stream, torch, pg, hbm_peak, clocks)
         wl.tau = args.tau
+        configs[f"decode_{args.ctx // 1024}k_ctx_{args.layers}_layers_tau_sweep"] = sweep
     del wl
     torch.cuda.empty_cache()
 
-    # ---------------- page-fill writer workload
-    writer = None
-    if not args.no_writer:
-        writer = bench_writer(args, device, stream, torch, bd, pg, hbm_peak)
+    writer = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, clocks=clocks)
+    if configs is not None:
+        configs.update(run_configs(args, device, stream, torch, bd, pg, hbm_peak, clocks, cfg_steps))
+    clk = clocks.stop()
 
     line = {
         "metric": METRIC, "value": us_step, "unit": "µs/step", "n_gpus": world, "steps": args.steps,
@@ -508,8 +538,15 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "packed_kv_gbs": job_rate(step_bytes, ms, world) / 1e9,
         "packed_kv_frac_of_peak": job_rate(step_bytes, ms, world) / 1e9 / (hbm_peak * world),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel (+ split combine)", "achieved": achieved,
-                     "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel + combine_kernel (one bd_decode_attention call)",
+                     "achieved": achieved_in_step, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved_in_step / hbm_peak,
+                     "frac_basis": (f"in step: one graph of the {args.layers} layers' decode calls alone (packed "
+                                    f"queries in place), {dec_graph_ms * 1000:.1f} us / {args.layers} = "
+                                    f"{in_step_ms * 1000:.2f} us per call"),
+                     "frac_in_step": achieved_in_step / hbm_peak, "us_per_call_in_step": in_step_ms * 1000,
+                     "frac_call": achieved_call / hbm_peak, "achieved_call": achieved_call,
+                     "us_per_call_alone": call_ms * 1000,
                      "traffic": decode_traffic(args), "bytes_per_launch": wl_bytes_note(args)},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "µs/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -519,13 +556,10 @@ def main():
         "launch": (f"one CUDA graph per step ({args.layers} x query, decode and split-combine kernels, "
                    "programmatic dependent launch)"),
         "clocks": clk,
+        "writer": writer,
     }
-    if tau_sweep:
-        line["tau_sweep_us_per_step"] = tau_sweep
-    if writer:
-        line["writer"] = writer
-    if args.suite:
-        line["suite"] = run_suite(args, device, stream, torch, bd, pg, hbm_peak)
+    if configs is not None:
+        line["configs"] = configs
     if rank == 0 and not args.no_cpu_baseline:
         smp = OracleDecodeSample(args.ctx, 256)
         runs = [smp.run() for _ in range(3)]
@@ -564,14 +598,16 @@ def decode_traffic(args):
     return DECODE_TRAFFIC["bytes"]
 
 
-def step_rate(wl, steps, warmup, stream, torch, pg, hbm_peak):
+def step_rate(wl, steps, warmup, stream, torch, pg, hbm_peak, clocks=None):
     """µs per step of a graphed decode step and its packed-KV bandwidth."""
-    ms = timed(graphed(lambda: wl.step(), torch), steps, warmup, stream, torch, pg)
+    ms = timed(graphed(lambda: wl.step(), torch), steps, warmup, stream, torch, pg, clocks)
+    ms = max_over_ranks(ms, pg, torch.device("cuda", torch.cuda.current_device()))
     gbs = wl.bytes_per_layer * wl.layers / (ms * 1e-3) / 1e9
-    return {"us_per_step": ms * 1000.0, "packed_kv_gbs": gbs, "frac_of_peak": gbs / hbm_peak}
+    return {"us_per_step": ms * 1000.0, "packed_kv_gbs": gbs, "frac_of_peak": gbs / hbm_peak,
+            "packed_bytes_per_step": wl.bytes_per_layer * wl.layers}
 
 
-def bench_append(args, device, stream, torch, bd, pg, hbm_peak):
+def bench_append(args, device, stream, torch, bd, pg, hbm_peak, clocks=None):
     """bd_append_kv for 64 sequences per layer: a step of 36 launches with no
     page completed, and one where every sequence completes a page (once
     every 128 decode steps)."""
@@ -603,27 +639,28 @@ def bench_append(args, device, stream, torch, bd, pg, hbm_peak):
                 bd.append_kv(ctx, l, t["kn"], t["vn"], sl, bt, t["sk"], t["sv"], t["tk"], t["tv"], 1.0, 1.0,
                              t["pool"])
 
-        ms = timed(graphed(step, torch), 100, args.warmup, stream, torch, pg)
+        ms = timed(graphed(step, torch), 100, args.warmup, stream, torch, pg, clocks)
         out[name + "_us_per_step"] = ms * 1000.0
     out["workload"] = f"{B} sequences x {layers} layers, one token each"
     out["page_fill_tok_per_s"] = B * 128 / (out["every_sequence_completes_a_page_us_per_step"] * 1e-6)
     return out
 
 
-def run_suite(args, device, stream, torch, bd, pg, hbm_peak):
-    """The other decode configurations, each a full 36-layer step."""
+def run_configs(args, device, stream, torch, bd, pg, hbm_peak, clocks, steps):
+    """The other configurations of the workload table, each a full step."""
     from nvfp4_kv_cache_bd_gb300 import synth
-    steps, out = 100, {}
-    wl = DecodeWorkload(32768, args.layers, 1.0, device)
-    out["decode_32k_ctx"] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak)
+    out = {}
+    wl = DecodeWorkload(4096, 1, 1.0, device)
+    r = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak, clocks)
+    r["note"] = ("4096-token context, 1 layer (the parity configuration): 4.6 MB of packed K/V, inside L2, so this "
+                 "is a latency figure, not a bandwidth one")
+    out["decode_4k_ctx_1_layer"] = r
     del wl
-    torch.cuda.empty_cache()
-    wl = DecodeWorkload(args.ctx, args.layers, 1.0, device)
-    sweep = {}
-    for tau in (0.0, 0.5, 4.0, 448.0):
-        wl.tau = tau
-        sweep[str(tau)] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak)
-    out[f"decode_{args.ctx // 1024}k_ctx_tau_sweep"] = sweep
+    out["writer_mxfp4"] = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=1, clocks=clocks)
+    wl = DecodeWorkload(32768, args.layers, 1.0, device)
+    assert wl.bytes_per_layer * wl.layers > L2_BYTES
+    out[f"decode_32k_ctx_{args.layers}_layers"] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak,
+                                                            clocks)
     del wl
     torch.cuda.empty_cache()
     lens = synth.log_uniform_lengths(32, 1024, 65536, 0)
@@ -632,12 +669,11 @@ def run_suite(args, device, stream, torch, bd, pg, hbm_peak):
         for recipe in (True, False):
             wl = DecodeWorkload(lens, args.layers, 1.0, device, fmt=fmt, recipe=recipe)
             batch[f"{fname}_{'rotation_centering' if recipe else 'plain_keys'}"] = step_rate(
-                wl, steps, args.warmup, stream, torch, pg, hbm_peak)
+                wl, steps, args.warmup, stream, torch, pg, hbm_peak, clocks)
             del wl
             torch.cuda.empty_cache()
-    out["decode_batch_32"] = batch
-    out["writer_mxfp4"] = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=1)
-    out["append"] = bench_append(args, device, stream, torch, bd, pg, hbm_peak)
+    out[f"decode_batch_32_{args.layers}_layers"] = batch
+    out["append"] = bench_append(args, device, stream, torch, bd, pg, hbm_peak, clocks)
     return out
 
 
@@ -646,7 +682,7 @@ def wl_bytes_note(args):
     return npages * HKV * 2 * 9216
 
 
-def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0):
+def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0, clocks=None):
     from nvfp4_kv_cache_bd_gb300 import synth
     seqs, layers = 64, args.layers
     ctx = bd.Context(bd.make_config(num_layers=layers, format=fmt))
@@ -665,7 +701,7 @@ def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0):
         for l in range(layers):
             bd.quantize_kv_pages(ctx, l, ks[l], vs[l], dst, gs[l][0], gs[l][1], pools[l])
 
-    ms = timed(graphed(step, torch), args.steps, args.warmup, stream, torch, pg)
+    ms = timed(graphed(step, torch), args.steps, args.warmup, stream, torch, pg, clocks)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(layers)]
     durs = []
     for _ in range(3):
