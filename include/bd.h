@@ -52,17 +52,24 @@
  *  KV pool of one layer: records ordered [physical page][kv head][K, V].
  *    record bytes R = 8192 + 128*nb, nb = 8 (NVFP4) or 4 (MXFP4):
  *    R = 9216 (NVFP4), 8704 (MXFP4).  bd_record_bytes() returns R.
- *    The K record:
- *      codes [128 tokens][64 B]: element d of a token's head vector is in
- *        byte d/2, even d in the low nibble.  Elements are in the rotated,
- *        centered domain when rotation / centering are on.
- *      scales[128 tokens][nb]: scale byte of block b of that token.
- *    The V record pairs token tau = 16 i + p with token tau + 8
+ *    The K record (the layout the decode's block-scaled tensor-core MMA
+ *    reads straight from shared memory):
+ *      codes: 128 tokens x 128 dims in groups of 8 tokens x 32 dims, each
+ *        group 128 contiguous bytes (16 per token): the byte of dims d, d+1
+ *        (d even, d in the low nibble) of token t is at
+ *        (t/8)*512 + (d/32)*128 + (t%8)*16 + (d%32)/2.  Elements are in the
+ *        rotated, centered domain when rotation / centering are on.
+ *      scales: nb/4 groups of 512 bytes (NVFP4 2, MXFP4 1), each 32 lines of
+ *        16 bytes; line i holds tokens i, i+32, i+64, i+96, four blocks each:
+ *        the byte of block b of token t is at
+ *        8192 + (b/4)*512 + (t%32)*16 + (t/32)*4 + b%4.
+ *    The V record pairs token tau = 16 i + 2 p with token tau + 1
  *    (16-token group i = 0..7, p = 0..7):
  *      codes [8 i][8 p][8 slots][16 B]: the byte of head dim d is
- *        code(tau, d) | code(tau + 8, d) << 4, at slot (d/16) XOR 2(p mod 4),
- *        byte d mod 16 of the slot.  (The XOR spreads the 16-byte reads of
- *        the decode's P V fragments over all shared-memory banks.)
+ *        code(tau, d) | code(tau + 1, d) << 4, at slot (d/16) XOR 2(p mod 4),
+ *        byte d mod 16 of the slot.  (A byte is one f16x2 of the decode's
+ *        P V operand; the XOR spreads its 16-byte reads over all
+ *        shared-memory banks.)
  *      scales[8 i][8 p][nb][2]: scale bytes of block b, token tau first.
  *    FP4 page p of a sequence holds its tokens 16 + 128 p ... 16 + 128 p + 127
  *    (tokens 0..15 are the BF16 sink).

@@ -78,16 +78,20 @@ def dequantize_pool(pool: np.ndarray, fmt: int, pages: np.ndarray, gk: float, gv
     nb = 8 if fmt == bd.FORMAT_NVFP4 else 4
     rb = 8192 + 128 * nb
     recs = pool.reshape(-1, H, 2, rb)[pages]                       # [n][H][2][rb]
-    kc = recs[:, :, 0, :8192].reshape(-1, H, 128, 64)
+    # K codes in groups of 8 tokens x 32 dims: [t//8][d//32][t%8][(d%32)//2] -> [t][d//2]
+    kc = recs[:, :, 0, :8192].reshape(-1, H, 16, 4, 8, 16).transpose(0, 1, 2, 4, 3, 5).reshape(-1, H, 128, 64)
     kcodes = np.stack([kc & 0xF, kc >> 4], axis=-1).reshape(-1, H, 128, 128)
-    ks = recs[:, :, 0, 8192:8192 + 128 * nb].reshape(-1, H, 128, nb)
+    # K scales: block b of token t at 8192 + (b//4)*512 + (t%32)*16 + (t//32)*4 + b%4
+    t = np.arange(128)[:, None]
+    b = np.arange(nb)[None, :]
+    ks = recs[:, :, 0, 8192 + (b // 4) * 512 + (t % 32) * 16 + (t // 32) * 4 + b % 4]
     k = _E2M1[kcodes] * np.repeat(_scale(fmt, ks), 128 // nb, axis=-1)
     vslot = recs[:, :, 1, :8192].reshape(-1, H, 8, 8, 8, 16)
     p = np.arange(8)[:, None]
     vc = vslot[:, :, :, p, np.arange(8)[None, :] ^ (2 * (p % 4))].reshape(-1, H, 8, 8, 128)
-    vcodes = np.concatenate([vc & 0xF, vc >> 4], axis=3).reshape(-1, H, 128, 128)   # tokens 16i + (p | p+8)
+    vcodes = np.stack([vc & 0xF, vc >> 4], axis=4).reshape(-1, H, 128, 128)   # tokens 16i + 2p + (0 | 1)
     vs = recs[:, :, 1, 8192:8192 + 128 * nb].reshape(-1, H, 8, 8, nb, 2)
-    vs = np.concatenate([vs[..., 0], vs[..., 1]], axis=3).reshape(-1, H, 128, nb)
+    vs = np.stack([vs[..., 0], vs[..., 1]], axis=4).reshape(-1, H, 128, nb)
     v = _E2M1[vcodes] * np.repeat(_scale(fmt, vs), 128 // nb, axis=-1)
     if fmt == bd.FORMAT_NVFP4:
         k, v = k * gk, v * gv

@@ -17,40 +17,43 @@
 // decode ends, so the next decode's producers fill their rings during this
 // one's tail.
 //
-// FP4 split CTA: warps 6 and 7 are producers.  One lane of each streams the
-// pages' K records (warp 6) or V records (warp 7), in page order, into its
-// own 6-slot shared-memory ring with cp.async.bulk (TMA, L2 evict-first),
-// completing on per-slot "full" mbarriers; each slot carries the index of
-// the page it holds, so a consumer never mistakes an older fill for its own.
-// Warps 0..5 consume: each takes the next page from a shared counter, so
-// every warp's pages increase and a page's softmax maximum never crosses
-// warps.  Per page a warp carries eight 16-token blocks through
-//  QK  : m16n8k16 f16 MMAs, M = 16 tokens, N = 8 = 4 query heads x 2 query
-//        terms, K = 16 head dims.  FP4 codes are widened by cvt e2m1x2->f16x2
-//        and multiplied by their E4M3 scale in f16, which is exact
-//        (E2M1 x E4M3 has at most 6 significant bits and lies in
-//        [2^-10, 2688]); the query terms are exact the same way.  Per-tensor
-//        scales, the 1/sqrt(128) softmax scale and q.mu are applied to the
-//        fp32 accumulators.  The K slot is released right after.
-//  P   : the page maximum m_p of every head (warp shuffles); P = exp(s - m_p);
-//        each 16-token block is quantized to FP4 with the amax2-or-amax6 rule;
-//        Phat = E2M1 x E4M3 / c is again exact in f16.  All of this happens
-//        before the page's V record is awaited.
-//  PV  : O^T[128 dims][8] += Vhat^T[dims][16 tokens] Phat^T.  The V record
-//        stores tokens tau and tau+8 in one byte, which is exactly an
-//        A-fragment register of this MMA; Phat reaches the B-fragment layout
-//        with two warp shuffles.
-//  Each warp merges its pages into a running (M, L, O); at the end the
-//  consumer warps' states are merged through shared memory into the split
-//  partial.
-// combine_kernel, one CTA per (sequence, query head), merges the splits:
-// O = sum 2^(m-M) O / sum 2^(m-M) l.
+// FP4 split CTA, two warpgroups with their own register shares:
+//  warp 0    streams the pages' K records, in page order, into a 4-slot
+//            shared-memory ring with cp.async.bulk (TMA, L2 evict-first);
+//  warp 1    streams the V records into a 6-slot V ring the same way;
+//  warp 2    computes every page's scores on the tensor core: the block-scaled
+//            tcgen05 MMA (kind::mxf4nvf4) takes the K record's FP4 codes
+//            (the B operand, N = the page's 128 tokens) and its E4M3 / UE8M0
+//            block scales straight from shared memory, the query (A operand,
+//            M = 128: 4 heads x 2 terms in lane quarter w, every other row
+//            zero) and its scales, and accumulates fp32 scores in tensor
+//            memory.  Pages go in rounds of four: page 4 r + w lands in lane
+//            quarter w of one 128-column score buffer (the first MMA of a
+//            round overwrites the buffer, the rest accumulate, and zero query
+//            rows leave the other quarters as they are);
+//  warp 3    owns the CTA's 256 TMEM columns (the score buffer, the query's
+//            and two pages' scale factors);
+//  warps 4-7 consume: warp 4 + w takes page 4 r + w of every round alone.
+//            One tcgen05 load (16x256b) gives lane (g, t) the scores of query
+//            head g (both terms) for tokens 8 j + 2 t, 8 j + 2 t + 1 -- the
+//            B-fragment layout of the P V MMA -- so the page maximum is a
+//            register reduction plus two shuffles, each 16-token block's FP4
+//            probabilities (amax2-or-amax6) are quantized in place, and P V
+//            runs as m16n8k16 f16 MMAs (O^T[128 dims][8] += Vhat^T Phat^T; V's
+//            scales run along head_dim, the MMA's output dimension, so a
+//            block-scaled MMA cannot take V).  Lanes of rows 4..7 carry no
+//            query head; their results are never read.
+// Every page's K and V record is read once from HBM; each page is processed
+// by one warp in a fixed order, so a split's result does not depend on
+// scheduling.  combine_kernel, one CTA per (sequence, query head), merges the
+// splits: O = sum 2^(m-M) O / sum 2^(m-M) l.
 //
 // The query, decode and combine kernels use programmatic dependent launch:
 // the producers start streaming pages while the query quantizer still runs;
 // every thread that reads the packed or raw query or the sink/tail rows, or
 // writes the workspace or out, first waits on the preceding grid.
 #include <math.h>
+#include <stddef.h>
 
 #include <mutex>
 
@@ -60,35 +63,68 @@ namespace bd {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kConsumers = 6;                    // consumer warps; warps 6 and 7 stream K and V
-constexpr int kThreads = (kConsumers + 2) * 32;
+constexpr int kConsumers = 4;                    // consumer warps 4..7, one TMEM lane quarter each
+constexpr int kFirstConsumer = 4;
+constexpr int kThreads = 256;
 constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
-constexpr int kNK = 6, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
+constexpr int kNK = 4, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
+constexpr int kCtasPerSm = 2;
+// Register split of an FP4 split CTA: launched at kLaunchRegs per thread,
+// the control warpgroup gives registers back (setmaxnreg.dec to kCtlRegs)
+// and the consumer warpgroup takes them (setmaxnreg.inc to kConsumerRegs).
+// The two shares add up exactly to the launch allocation; the host refuses
+// to launch if the compiled kernel's register count differs, because an
+// increase beyond the launch allocation would wait forever.
+constexpr int kLaunchRegs = 128, kCtlRegs = 40, kConsumerRegs = 2 * kLaunchRegs - kCtlRegs;
+static_assert(kCtlRegs % 8 == 0 && kConsumerRegs % 8 == 0 && kConsumerRegs <= 256, "setmaxnreg counts");
 constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
 constexpr int kWavePages = 32;   // one-wave splits up to this many pages ...
 constexpr int kBatchPages = 16;  // ... else splits of this many (more if kMaxSplits needs it)
-constexpr int kMaxSplits = 43;    // splits + 1 per (sequence, kv head); the combine stages them in 22.7 KB
+constexpr int kMaxSplits = 64;    // splits + 1 per (sequence, kv head); the combine stages them in 33.8 KB
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
+// Tensor memory of an FP4 split CTA (256 columns): the score buffer at
+// columns 0..127 (one column per token of the page), the query's scale
+// factors at 128 (+16 for the second NVFP4 group), and two slots of a page's
+// K scale factors at 160 + 32 s (+16).  Every scale-factor address starts on
+// a 16-column boundary.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kSfaCol = 128;
+__device__ __forceinline__ uint32_t sfb_col(int slot, int j) { return 160u + 32u * slot + 16u * j; }
+constexpr int kN = 128;                          // MMA N: the page's tokens
+// The query operand: 28 core-matrix groups of 8 rows x 64 B, all zero but
+// groups 12 (rows 0..3: term 1 of heads 0..3) and 13 (rows 0..3: term 2).
+// For lane quarter w the descriptor starts 4 w groups before group 12, so
+// its rows 32 w .. 32 w + 15 are the query and all other rows zero.
+constexpr int kQiGroups = 28, kQiFirst = 12;
+
 struct alignas(16) Ctl {
-    unsigned long long fullK[kNK], emptyK[kNK];   // K ring
-    unsigned long long fullV[kNV], emptyV[kNV];   // V ring
+    unsigned long long fullK[kNK], emptyK[kNK];   // K ring (empty: the page's MMAs completed)
+    unsigned long long fullV[kNV], emptyV[kNV];   // V ring (empty: the page's consumer warp)
+    unsigned long long accFull;                   // a round's scores are in the buffer
+    unsigned long long accEmpty;                  // all four consumer warps have read the round
+    unsigned long long sfbFree[2];                // a K scale-factor slot's MMAs completed
+    unsigned long long mmaDone;                   // every MMA the CTA issued has completed
     float wm[kConsumers + 1][4];   // per-warp running max per head (log2 units); last: BF16 tokens
     float wl[kConsumers + 1][4];   // per-warp softmax denominator per head
     int abort_flag;
-    int next_page;             // next page index a consumer warp takes
-    int tagK[kNK], tagV[kNV];  // page index each slot's latest fill holds (-1: none)
-    int badK[kNK];             // 1: that fill's block-table entry was out of range (no data, skip the page)
+    int tagK[kNK], tagV[kNV];      // page index each slot's latest fill holds (-1: none)
+    uint32_t tmem;                 // TMEM base address
 };
-constexpr int kPTabBytes = 2 * 128 * 4;                        // scale tables (see decode_kernel)
-constexpr int kSmemBytes = kRingBytes + (int)sizeof(Ctl) + kPTabBytes;
+constexpr int kCtlBytes = (int)((sizeof(Ctl) + 127) / 128 * 128);
+constexpr int kTabOff = kRingBytes + kCtlBytes;      // probability-quantizer tables (1 KB)
+constexpr int kQiOff = kTabOff + 1024;               // query operand image (28 x 512 B)
+constexpr int kSfaOff = kQiOff + kQiGroups * 512;    // query scale-factor groups (2 x 512 B)
+constexpr int kSmemBytes = kSfaOff + 1024;
+static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+static_assert(kRingBytes % 128 == 0 && kTabOff % 128 == 0 && kQiOff % 128 == 0 && kSfaOff % 128 == 0 &&
+                  kMaxRec % 128 == 0,
+              "ring slots, tables and operand areas start on 128-byte boundaries");
 // Merge area in the (drained) ring: the O of each consumer warp and of the
 // BF16 tokens, [kConsumers + 1][4 heads][128] floats; the BF16 staging follows.
 constexpr int kStateBytes = (kConsumers + 1) * 4 * 128 * 4;
-static_assert(kStateBytes + 2 * 143 * 272 + (4 * 128 + 4 * 144 + 8) * 4 <= kRingBytes,
+static_assert(kStateBytes + 143 * 272 + (4 * 128 + 4 * 144) * 4 <= kRingBytes,
               "states and sink/tail staging must fit the ring");
-static_assert(sizeof(Ctl) % 16 == 0, "the tables after Ctl must stay 16-byte aligned");
-static_assert(kMaxSplits <= 64, "the combine handles two splits per lane");
 
 __device__ __forceinline__ float ex2(float x) {
     float r;
@@ -98,16 +134,8 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned).
-
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
-
-// 16-bit pair of code bytes (bytes 2k, 2k+1) from a 16-byte chunk.
-__device__ __forceinline__ uint32_t byte_pair(const uint4& c, int k) {
-    const uint32_t wd = (k < 2) ? c.x : (k < 4) ? c.y : (k < 6) ? c.z : c.w;
-    return (k & 1) ? (wd >> 16) : (wd & 0xFFFFu);
-}
 
 // f16 bits of 2^k for k <= 0 (subnormal below -14, zero below -24).
 __device__ __forceinline__ uint32_t f16_pow2(int k) {
@@ -144,38 +172,6 @@ __device__ __forceinline__ bool wait_stage_page(uint32_t bar, uint32_t parity, c
     }
 }
 
-// Element-wise maximum of v[0..7] over the 8 lanes that share lane & 3 (lane
-// bits 2..4), left in every one of them: a reduce-scatter (4 + 2 + 1
-// shuffles) leaves each lane the full maximum of one element, an all-gather
-// (1 + 2 + 4) returns all eight.  14 shuffles instead of 3 per element.
-__device__ __forceinline__ void max8_across_g(float* v, int lane) {
-    const bool b2 = lane & 16, b1 = lane & 8, b0 = lane & 4;
-    float h4[4];   // elements (b2 ? 4 : 0) + 0..3
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float send = b2 ? v[j] : v[j + 4], keep = b2 ? v[j + 4] : v[j];
-        h4[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, 16));
-    }
-    float h2[2];   // elements (b2 ? 4 : 0) + (b1 ? 2 : 0) + 0..1
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const float send = b1 ? h4[j] : h4[j + 2], keep = b1 ? h4[j + 2] : h4[j];
-        h2[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, 8));
-    }
-    // element (b2 ? 4 : 0) + (b1 ? 2 : 0) + (b0 ? 1 : 0), now over all 8 lanes
-    const float h1 = fmaxf(b0 ? h2[1] : h2[0], __shfl_xor_sync(kFull, b0 ? h2[0] : h2[1], 4));
-    const float o1 = __shfl_xor_sync(kFull, h1, 4);
-    const float g2[2] = {b0 ? o1 : h1, b0 ? h1 : o1};
-    const float o2[2] = {__shfl_xor_sync(kFull, g2[0], 8), __shfl_xor_sync(kFull, g2[1], 8)};
-    const float g4[4] = {b1 ? o2[0] : g2[0], b1 ? o2[1] : g2[1], b1 ? g2[0] : o2[0], b1 ? g2[1] : o2[1]};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float o4 = __shfl_xor_sync(kFull, g4[j], 16);
-        v[j] = b2 ? o4 : g4[j];
-        v[j + 4] = b2 ? g4[j] : o4;
-    }
-}
-
 // ------------------------------------------------------ BF16 sink + tail --
 
 // Shared-memory row pitch of a staged bf16 head vector: 256 B plus 16 B so
@@ -204,22 +200,23 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
         return;
     }
     float* so = reinterpret_cast<float*>(smem) + kConsumers * 4 * kD;   // this state's O
-    uint8_t* ks = smem + kStateBytes;                              // [T][272 B] bf16 keys
-    uint8_t* vs = ks + kMaxBf16Tok * kRowPitch;                    // [T][272 B] bf16 values
-    float* qf = reinterpret_cast<float*>(vs + kMaxBf16Tok * kRowPitch);   // [4][128]
+    uint8_t* rows = smem + kStateBytes;                            // [T][272 B] bf16 keys, later values
+    float* qf = reinterpret_cast<float*>(rows + kMaxBf16Tok * kRowPitch);   // [4][128]
     float* sp = qf + 4 * kD;                                       // [4][144] scores, then P
-    // stage the sink and tail rows of this kv head with asynchronous 16-byte
-    // copies (no thread waits for one load before issuing the next)
-    for (int i = tid; i < T * 16; i += blockDim.x) {
-        const int tau = i >> 4, c = i & 15;
-        const size_t krow = tau < ns ? (((size_t)b * kSink + tau) * a.hkv + h) * kD
-                                     : (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
-        const uint16_t* kb = (tau < ns ? a.sink_k : a.tail_k) + krow + 8 * c;
-        const uint16_t* vb = (tau < ns ? a.sink_v : a.tail_v) + krow + 8 * c;
-        cp_async16(smem_u32(ks + tau * kRowPitch + 16 * c), kb);
-        cp_async16(smem_u32(vs + tau * kRowPitch + 16 * c), vb);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
+    // stage the rows of this kv head (keys now, values after the scores) with
+    // asynchronous 16-byte copies (no thread waits for one load before
+    // issuing the next)
+    auto stage = [&](const uint16_t* sink, const uint16_t* tail) {
+        for (int i = tid; i < T * 16; i += blockDim.x) {
+            const int tau = i >> 4, c = i & 15;
+            const size_t row = tau < ns ? (((size_t)b * kSink + tau) * a.hkv + h) * kD
+                                        : (((size_t)b * kPage + (tau - ns)) * a.hkv + h) * kD;
+            cp_async16(smem_u32(rows + tau * kRowPitch + 16 * c), (tau < ns ? sink : tail) + row + 8 * c);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    stage(a.sink_k, a.tail_k);
+    const uint8_t* ks = rows;
     if (tid < 4 * kD / 8) {
         const int hh = tid >> 4, c = tid & 15;
         const uint4 u = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.hq + 4 * h + hh) * kD + 8 * c);
@@ -269,6 +266,8 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
         }
     }
     __syncthreads();
+    stage(a.sink_v, a.tail_v);   // the keys are no longer read: the values take their place
+    const uint8_t* vs = rows;
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < 4) {
         float m = -INFINITY;
@@ -288,6 +287,7 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
             ctl->wl[kConsumers][warp] = l;
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     // O = P V: thread (head dim d, head pair hp), all 256 threads
     {
@@ -306,98 +306,189 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
     }
 }
 
-// ------------------------------------------------ FP4 page split: consumer --
+// ------------------------------------------------ FP4 page split: the MMA --
 
+// Lane 0 of warp 2: the query's scale factors into TMEM, then per round of
+// four pages (page 4 r + w into lane quarter w) each page's K scale factors
+// and its two K = 64 MMAs, S^T = Q K^T with the query operand offset so that
+// only quarter w's rows are nonzero.
+template <int FMT>
+__device__ void mma_rounds(const DecodeArgs& a, int n, const int32_t* bt, uint8_t* smem, Ctl* ctl) {
+    constexpr int kGroups = (FMT == BD_FORMAT_NVFP4) ? 2 : 1;
+    constexpr uint32_t LBO = 128, SBO = 512;
+    const uint32_t tm = ctl->tmem;
+    tc_fence_after();
+    for (int j = 0; j < kGroups; ++j) tmem_cp_sf(tm + kSfaCol + 16 * j, smem_u32(smem + kSfaOff + 512 * j));
+    const uint32_t qimg = smem_u32(smem + kQiOff + kQiFirst * 512);
+    const int rounds = (n + 3) / 4;
+    bool aborted = false;
+    for (int r = 0; r < rounds && !aborted; ++r) {
+        // the consumers have read the previous round's scores
+        if (r > 0 && !mbar_wait_bounded(smem_u32(&ctl->accEmpty), (r - 1) & 1, kWaitLimitNs, &ctl->abort_flag)) {
+            aborted = true;
+            break;
+        }
+        bool first = true;
+        for (int w = 0; w < 4; ++w) {
+            const int k = 4 * r + w;
+            if (k >= n) break;
+            const int s = k % kNK, slot = k & 1;
+            if (!wait_stage_page(smem_u32(&ctl->fullK[s]), (k / kNK) & 1, &ctl->tagK[s], k, &ctl->abort_flag)) {
+                aborted = true;
+                break;
+            }
+            // the scale-factor slot's previous MMAs (page k - 2) have completed
+            if (k >= 2 && !mbar_wait_bounded(smem_u32(&ctl->sfbFree[slot]), ((k >> 1) - 1) & 1, kWaitLimitNs,
+                                             &ctl->abort_flag)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            if (page_ok(bt[k], a.pool_pages)) {
+                const uint32_t ks = smem_u32(smem + s * kMaxRec);
+                for (int j = 0; j < kGroups; ++j) tmem_cp_sf(tm + sfb_col(slot, j), ks + kCodeBytes + 512 * j);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    // dims 64 j .. 64 j + 63: core-matrix columns 2 j, 2 j + 1
+                    const uint64_t ad = smem_desc(qimg - 4 * w * SBO + 2 * j * LBO, LBO, SBO);
+                    const uint64_t bdsc = smem_desc(ks + 2 * j * LBO, LBO, SBO);
+                    const uint32_t acc = (first && j == 0) ? 0u : 1u;
+                    if (FMT == BD_FORMAT_NVFP4) {
+                        mma_nvf4(tm, ad, bdsc, mma_idesc_e2m1(kN, false, 0), tm + kSfaCol + 16 * j,
+                                 tm + sfb_col(slot, j), acc);
+                    } else {
+                        // one scale-factor group holds all four 32-dim blocks:
+                        // MMA j reads bytes 2 j, 2 j + 1 of each word
+                        mma_mxf4(tm, ad, bdsc, mma_idesc_e2m1(kN, true, 2 * j), tm + kSfaCol, tm + sfb_col(slot, 0),
+                                 acc);
+                    }
+                }
+                first = false;
+                tc_commit(smem_u32(&ctl->sfbFree[slot]));
+                tc_commit(smem_u32(&ctl->emptyK[s]));
+            } else {
+                // an entry outside the pool: no data arrived, nothing to multiply
+                mbar_arrive(smem_u32(&ctl->sfbFree[slot]));
+                mbar_arrive(smem_u32(&ctl->emptyK[s]));
+            }
+        }
+        if (aborted) break;
+        tc_commit(smem_u32(&ctl->accFull));
+    }
+    if (aborted) {
+        if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
+        ctl->abort_flag = 1;
+    }
+    // every MMA issued has finished before the CTA reuses its shared memory
+    // or frees the tensor memory
+    tc_commit(smem_u32(&ctl->mmaDone));
+    (void)mbar_wait_bounded(smem_u32(&ctl->mmaDone), 0, kWaitLimitNs, nullptr);
+}
+
+// Warp 2 of an FP4 split CTA.  The whole warp builds the query operand: the
+// zero image with group 12 = term 1 and group 13 = term 2 of query heads
+// 4h .. 4h+3 (rows 0..3 of each group, core-matrix order: LBO 128 B along K,
+// SBO 512 B between groups), and its scale factors as TMEM scale-factor
+// groups (lines 0..3 and 8..11, the same word for all four lane quarters).
+// Lane 0 then issues the MMAs.
+template <int FMT>
+__device__ void issue_qk(const DecodeArgs& a, int b, int h, int n, const int32_t* bt, uint8_t* smem, Ctl* ctl,
+                         int lane) {
+    griddep_wait();   // the packed query may come from the preceding grid
+    const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
+    const int hq = a.hq;
+    uint8_t* Qi = smem + kQiOff;
+    uint8_t* Sf = smem + kSfaOff;
+    for (int i = lane; i < kQiGroups * 512 / 16; i += 32) reinterpret_cast<uint4*>(Qi)[i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(Sf)[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(Sf)[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    {
+        const int row = lane >> 2, ch = lane & 3;   // (term, head) x 4 chunks of 32 dims
+        const int term = row >> 2, hh = row & 3;
+        *reinterpret_cast<uint4*>(Qi + (kQiFirst + term) * 512 + ch * 128 + hh * 16) =
+            *reinterpret_cast<const uint4*>(qrec + (term * hq + 4 * h + hh) * 64 + 16 * ch);
+        if (lane < 8) {
+            // lane = (term st, head sh); A row 32 w + line: line sh is term 1,
+            // line 8 + sh term 2
+            const int st = lane >> 2, sh = lane & 3;
+            const int line = (st == 0 ? 0 : 8) + sh;
+            if (FMT == BD_FORMAT_NVFP4) {
+                const uint2 s = *reinterpret_cast<const uint2*>(qrec + 2 * hq * 64 + (st * hq + 4 * h + sh) * 8);
+                *reinterpret_cast<uint4*>(Sf + 16 * line) = make_uint4(s.x, s.x, s.x, s.x);         // blocks 0..3
+                *reinterpret_cast<uint4*>(Sf + 512 + 16 * line) = make_uint4(s.y, s.y, s.y, s.y);   // blocks 4..7
+            } else {
+                const uint32_t s = *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (st * hq + 4 * h + sh) * 4);
+                *reinterpret_cast<uint4*>(Sf + 16 * line) = make_uint4(s, s, s, s);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mma_rounds<FMT>(a, n, bt, smem, ctl);
+}
+
+// ------------------------------------------ FP4 page split: the consumers --
+
+// Warps 4..7 of an FP4 split CTA (w = warp - 4): page 4 r + w of every round,
+// read from lane quarter w of the score buffer.  Lane (g, t) holds query head
+// g (g < 4; rows 4..7 are zero and their lanes compute nothing that is
+// read) for the page's tokens 8 j + 2 t + e (j = 0..15, e = 0, 1).  Running
+// state per lane: its head's maximum M and its tokens' share of the
+// denominator l; O^T as m16n8 accumulator tiles (dims permuted as in the V
+// record: lane (g, t) holds dims 16 g .. 16 g + 15 of heads 2 t, 2 t + 1 when
+// t < 2).
 template <int FMT, int PM>
-__device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t* smem, Ctl* ctl, int warp,
-                              int lane) {
+__device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, const int32_t* bt, uint8_t* smem, Ctl* ctl,
+                              int w, int lane) {
     const int g = lane >> 2, t = lane & 3;
     griddep_wait();
     const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
     const int hq = a.hq;
-    // B fragments of the query: row n = g -> head 4h + g/2, term g%2; this
-    // lane's k-slots are head dims 32t .. 32t+31.
-    uint32_t qB[16];
-    float qx[2];   // MXFP4: 2^(reference exponent) of this lane's two C columns
-    {
-        const int jq = 4 * h + (g >> 1), term = g & 1;
-        const uint4 qc = *reinterpret_cast<const uint4*>(qrec + (term * hq + jq) * 64 + 16 * t);
-        uint32_t slo, shi;
-        if (FMT == BD_FORMAT_NVFP4) {
-            const uint32_t qsd = e4m3x2_to_f16x2(
-                *reinterpret_cast<const uint16_t*>(qrec + 2 * hq * 64 + (term * hq + jq) * 8 + 2 * t));
-            slo = bcast_lo(qsd);
-            shi = bcast_hi(qsd);
-        } else {
-            const uint32_t e4 = *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term * hq + jq) * 4);
-            int emax = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) emax = max(emax, (int)((e4 >> (8 * q)) & 0xFF));
-            slo = shi = bcast_lo(f16_pow2((int)((e4 >> (8 * t)) & 0xFF) - emax));
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t pr = byte_pair(qc, kk);
-            const uint32_t sc = kk < 4 ? slo : shi;
-            qB[2 * kk] = hmul2(e2m1x2_to_f16x2(pr & 0xFF), sc);
-            qB[2 * kk + 1] = hmul2(e2m1x2_to_f16x2(pr >> 8), sc);
-        }
-        qx[0] = qx[1] = 1.0f;
-        if (FMT == BD_FORMAT_MXFP4) {
-#pragma unroll
-            for (int term2 = 0; term2 < 2; ++term2) {
-                const uint32_t e4 =
-                    *reinterpret_cast<const uint32_t*>(qrec + 2 * hq * 64 + (term2 * hq + 4 * h + t) * 4);
-                int emax = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) emax = max(emax, (int)((e4 >> (8 * q)) & 0xFF));
-                qx[term2] = pow2i(emax - 127);
-            }
-        }
-    }
     const float* gq = reinterpret_cast<const float*>(qrec + 2 * hq * 64 + 2 * hq * 8);
-    const float gK = (FMT == BD_FORMAT_NVFP4) ? a.gk : 1.0f;
+    // score = a1 * (Q1 . K) + a2 * (Q2 . K) + q.mu, in log2 units (MXFP4:
+    // the MMA applied every scale already)
+    const float a1 = (FMT == BD_FORMAT_NVFP4) ? kSmLog2e * a.gk * gq[0] : kSmLog2e;
+    const float a2 = (FMT == BD_FORMAT_NVFP4) ? kSmLog2e * a.gk * gq[1] : kSmLog2e;
+    const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + (g & 3)] : 0.0f;
     const float gV = (FMT == BD_FORMAT_NVFP4) ? a.gv : 1.0f;
-    const float a1 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[0] : qx[0]);
-    const float a2 = kSmLog2e * gK * ((FMT == BD_FORMAT_NVFP4) ? gq[1] : qx[1]);
-    const float bq = a.centering ? kSmLog2e * gq[4 + 4 * h + t] : 0.0f;
     const float ccf = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
     const float tau = a.tau;
-    // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c)
-    // f16x2
-    const float* ptab_rcp = reinterpret_cast<const float*>(smem + kRingBytes + sizeof(Ctl));
+    // per-byte tables (see decode_kernel): [0,128) 1/sd, [128,256) (sd/c, sd/c) f16x2
+    const float* ptab_rcp = reinterpret_cast<const float*>(smem + kTabOff);
     const uint32_t* ptab_sdc = reinterpret_cast<const uint32_t*>(ptab_rcp + 128);
-    const int srcA = (lane & ~3) | ((2 * t) & 3), srcB = (lane & ~3) | ((2 * t + 1) & 3);
-    const int gs = g & 3;
+    const uint32_t tm_quarter = ctl->tmem + ((uint32_t)(32 * w) << 16);
+    // this lane's O columns are heads 2t, 2t+1 (t < 2): lanes 8t and 8t + 4 hold them
+    const int srcA = (8 * t) & 31, srcB = (8 * t + 4) & 31;
 
-    float Mt = -INFINITY, MA = -INFINITY, MB = -INFINITY;   // running max of heads t, 2t, 2t+1
-    float lacc = 0.0f;
+    float M = -INFINITY, l = 0.0f;
     float o[8][4];
 #pragma unroll
     for (int bm = 0; bm < 8; ++bm) o[bm][0] = o[bm][1] = o[bm][2] = o[bm][3] = 0.0f;
 
-    for (;;) {
-        // the next page in order: warps take pages as they become free, so
-        // every warp's pages increase and the lowest unfinished page can
-        // always proceed
-        int k = 0;
-        if (lane == 0) k = atomicAdd(&ctl->next_page, 1);
-        k = __shfl_sync(kFull, k, 0);
-        if (k >= n) break;
-        const int sk = k % kNK, sv = k % kNV;
-        // A warp may start waiting for fill j of a slot before fill j-1 has
-        // landed; the phase parity alone cannot tell fill j-2 from fill j, the
-        // page tag can.
-        if (!wait_stage_page(smem_u32(&ctl->fullK[sk]), (k / kNK) & 1, &ctl->tagK[sk], k, &ctl->abort_flag)) {
+    const int rounds = (n + 3) / 4;
+    for (int r = 0; r < rounds; ++r) {
+        const int k = 4 * r + w;
+        const bool has = k < n;
+        const bool ok = has && page_ok(bt[k], a.pool_pages);
+        if (!mbar_wait_bounded(smem_u32(&ctl->accFull), r & 1, kWaitLimitNs, &ctl->abort_flag)) {
             if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
             ctl->abort_flag = 1;
             break;
         }
-        if (ctl->badK[sk]) {
-            // out-of-range block-table entry: nothing was copied for this page
-            // and it is left out; hand both slots back in ring order
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyK[sk]));
+        uint32_t raw[64];
+        if (ok) {
+            tc_fence_after();
+            tmem_ld_16x256b_x16(tm_quarter, raw);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->accEmpty));
+        if (!has) continue;
+        const int sv = k % kNV;
+        if (!ok) {
+            // out-of-range block-table entry: no data, the page is left out;
+            // hand its V slot back in ring order
             if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
                 if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
                 ctl->abort_flag = 1;
@@ -407,99 +498,35 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
             if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyV[sv]));
             continue;
         }
-        const uint8_t* Ks = smem + sk * kMaxRec;
-        const uint8_t* Vs = smem + (kNK + sv) * kMaxRec;
 
-        // ---------------- QK over the eight 16-token blocks: log2-scaled
-        // scores of head t for tokens 16mi+g and 16mi+g+8 stay in registers
-        float sc[16];
-        float mp = -INFINITY;
+        // ---------------- scores of head g, tokens 8 j + 2 t + e, log2 units
+        float s[32];
 #pragma unroll
-        for (int mi = 0; mi < 8; ++mi) {
-            {
-                const int tok0 = 16 * mi + g, tok1 = tok0 + 8;
-                const uint4 c0 = lds128(Ks + tok0 * 64 + 16 * t);
-                const uint4 c1 = lds128(Ks + tok1 * 64 + 16 * t);
-                uint32_t s0lo, s0hi, s1lo, s1hi;
-                float fk0 = 1.0f, fk1 = 1.0f;
-                if (FMT == BD_FORMAT_NVFP4) {
-                    // scale bytes of blocks 2t, 2t+1 of both rows, one 16-bit
-                    // load per row, widened exactly to f16 and broadcast to
-                    // (sd, sd) pairs
-                    const uint32_t h0 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok0 * 8 + 2 * t));
-                    const uint32_t h1 = e4m3x2_to_f16x2(lds16(Ks + kCodeBytes + tok1 * 8 + 2 * t));
-                    s0lo = bcast_lo(h0);
-                    s0hi = bcast_hi(h0);
-                    s1lo = bcast_lo(h1);
-                    s1hi = bcast_hi(h1);
-                } else {
-                    const int e0 = Ks[kCodeBytes + tok0 * 4 + t], e1 = Ks[kCodeBytes + tok1 * 4 + t];
-                    int m0 = max(e0, __shfl_xor_sync(kFull, e0, 1));
-                    m0 = max(m0, __shfl_xor_sync(kFull, m0, 2));
-                    int m1 = max(e1, __shfl_xor_sync(kFull, e1, 1));
-                    m1 = max(m1, __shfl_xor_sync(kFull, m1, 2));
-                    s0lo = s0hi = bcast_lo(f16_pow2(e0 - m0));
-                    s1lo = s1hi = bcast_lo(f16_pow2(e1 - m1));
-                    fk0 = pow2i(m0 - 127);
-                    fk1 = pow2i(m1 - 127);
-                }
-                // two accumulators halve the dependent MMA chain of the block
-                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t cw0[4] = {c0.x, c0.y, c0.z, c0.w}, cw1[4] = {c1.x, c1.y, c1.z, c1.w};
+        for (int j = 0; j < 16; ++j)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // word j holds bytes 4j..4j+3: k-tiles 2j (bytes 4j, 4j+1) and 2j+1
-                    uint32_t f0[4], f1[4];
-                    e2m1x8_to_f16x2x4(cw0[j], f0);
-                    e2m1x8_to_f16x2x4(cw1[j], f1);
-                    const uint32_t sa = j < 2 ? s0lo : s0hi, sb2 = j < 2 ? s1lo : s1hi;
-                    uint32_t A[4];
-                    A[0] = hmul2(f0[0], sa);
-                    A[1] = hmul2(f1[0], sb2);
-                    A[2] = hmul2(f0[1], sa);
-                    A[3] = hmul2(f1[1], sb2);
-                    mma16816(acc, A, qB[4 * j], qB[4 * j + 1]);
-                    A[0] = hmul2(f0[2], sa);
-                    A[1] = hmul2(f1[2], sb2);
-                    A[2] = hmul2(f0[3], sa);
-                    A[3] = hmul2(f1[3], sb2);
-                    mma16816(acc2, A, qB[4 * j + 2], qB[4 * j + 3]);
-                }
+            for (int e = 0; e < 2; ++e)
+                s[2 * j + e] = fmaf(__uint_as_float(raw[4 * j + 2 + e]), a2, fmaf(__uint_as_float(raw[4 * j + e]), a1, bq));
+
+        // ---------------- page maximum: 32 in registers, then the 4 lanes t
+        float mp = s[0];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-                const float s0 = fmaf(fk0, fmaf(acc[1], a2, acc[0] * a1), bq);
-                const float s1 = fmaf(fk1, fmaf(acc[3], a2, acc[2] * a1), bq);
-                sc[2 * mi] = s0;
-                sc[2 * mi + 1] = s1;
-                mp = fmaxf(mp, fmaxf(s0, s1));
-            }
+        for (int i = 1; i < 32; ++i) mp = fmaxf(mp, s[i]);
+        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 1));
+        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 2));
+
+        // ---------------- running state: new maximum, page weight, rescale
+        const float mn = fmaxf(M, mp);
+        const float alpha = ex2(M - mn), wpage = ex2(mp - mn);
+        M = mn;
+        float pr[32], lp = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            pr[i] = ex2(s[i] - mp);   // P relative to the page's own maximum
+            lp += pr[i];
         }
-
-        // the K slot is free once every lane's key reads are done
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyK[sk]));
-
-        // ---------------- page maximum of head t (and of heads 2t, 2t+1)
-        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 4));
-        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 8));
-        mp = fmaxf(mp, __shfl_xor_sync(kFull, mp, 16));
-        const float mpA = __shfl_sync(kFull, mp, srcA), mpB = __shfl_sync(kFull, mp, srcB);
-
-        // ---------------- per 16-token block: probabilities and their FP4
-        // quantization into P V's B fragments, all before the page's V record
-        // is awaited (its slot is held only for P V).  NVFP4: the running max
-        // is updated first and
-        // the page weight 2^(m_p - M) is folded into the f16 Phat operand, so
-        // P V accumulates straight into O (one f16 rounding, < 2^-11
-        // relative, per weighted Phat).  MXFP4 keeps a per-page O_p because
-        // its V reference exponent changes from page to page.
-        const float mnt = fmaxf(Mt, mp);
-        const float wpage = ex2(mp - mnt);
-        uint32_t wh = 0x3C003C00u;   // (1, 1)
-        float op[8][4];
+        l = fmaf(l, alpha, wpage * lp);
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcB);
         if (FMT == BD_FORMAT_NVFP4) {
-            const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
-            const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
             if (__any_sync(kFull, (aA != 1.0f) | (aB != 1.0f))) {
 #pragma unroll
                 for (int bm = 0; bm < 8; ++bm) {
@@ -509,68 +536,55 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
                     o[bm][3] *= aB;
                 }
             }
-            MA = mnA;
-            MB = mnB;
-            wh = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(wpage)));
-        } else {
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
-        }
-        // the page's probabilities first, then the eight blocks' maxima of
-        // u = c P over their 16 tokens with one reduction across the lanes g
-        float pr[16];
-        float lpage = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            pr[2 * i] = ex2(sc[2 * i] - mp);
-            pr[2 * i + 1] = ex2(sc[2 * i + 1] - mp);
-            lpage += pr[2 * i] + pr[2 * i + 1];
-        }
-        float bmax[8];
-        uint32_t bfr[16];   // B fragments of Phat for P V, two per block
-        if (PM != BD_P_NONE) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) bmax[i] = fmaxf(pr[2 * i] * ccf, pr[2 * i + 1] * ccf);
-            max8_across_g(bmax, lane);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            {
-                const float p0 = pr[2 * i], p1 = pr[2 * i + 1];
-                uint32_t pv;
-                if (PM == BD_P_NONE) {
-                    const __half2 hh = __floats2half2_rn(p0, p1);
-                    pv = *reinterpret_cast<const uint32_t*>(&hh);
-                } else {
-                    const float u0 = p0 * ccf, u1 = p1 * ccf;
-                    const float am = bmax[i];
-                    const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (am < tau);
-                    const float sv = two ? am * 0.5f : div6(am);
-                    // scale byte -> 1/sd (correctly rounded) and (sd/c, sd/c) from the tables;
-                    // byte 0 is the zero scale (S == 0: all codes zero)
-                    const uint32_t sbyte = e4m3(sv);
-                    const float inv = ptab_rcp[sbyte];
-                    const uint32_t byte = (sbyte == 0) ? 0u : e2m1x2(__fmul_rn(u0, inv), __fmul_rn(u1, inv));
-                    pv = hmul2(e2m1x2_to_f16x2(byte), ptab_sdc[sbyte]);
-                }
-                if (FMT == BD_FORMAT_NVFP4) pv = hmul2(pv, wh);
-                // lanes with g >= 4 feed the padding columns 4..7 (duplicates of
-                // heads 0..3); their outputs are never read
-                bfr[2 * i] = __shfl_sync(kFull, pv, 4 * t + gs);
-                bfr[2 * i + 1] = __shfl_sync(kFull, pv, 16 + 4 * t + gs);
-            }
         }
 
-        // ---------------- P V: only now is the page's V record needed
+        // ---------------- FP4 probabilities: 16-token block i is j = 2i, 2i+1
+        // of the four lanes t; the f16x2 of pair j is the P V B-fragment
+        // register of k-tile j / 2 (low: token 8 j + 2 t)
+        uint32_t ph[16];
+        if (PM == BD_P_NONE) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const __half2 hh = __floats2half2_rn(pr[2 * j], pr[2 * j + 1]);
+                ph[j] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = pr[4 * i + e] * ccf;
+                float bm = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+                const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (bm < tau);
+                const uint32_t sb = e4m3(two ? bm * 0.5f : div6(bm));
+                const float inv = ptab_rcp[sb];   // 0 for the zero scale: all codes 0
+                const uint32_t sdc = ptab_sdc[sb];
+                ph[2 * i] = hmul2(e2m1x2_to_f16x2(e2m1x2(__fmul_rn(u[0], inv), __fmul_rn(u[1], inv))), sdc);
+                ph[2 * i + 1] = hmul2(e2m1x2_to_f16x2(e2m1x2(__fmul_rn(u[2], inv), __fmul_rn(u[3], inv))), sdc);
+            }
+        }
+        if (FMT == BD_FORMAT_NVFP4) {
+            // fold the page weight 2^(m_p - M) into Phat: P V accumulates straight into O
+            const uint32_t wh = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(wpage)));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ph[j] = hmul2(ph[j], wh);
+        }
+
+        // ---------------- P V over the page's eight 16-token groups
         if (!wait_stage_page(smem_u32(&ctl->fullV[sv]), (k / kNV) & 1, &ctl->tagV[sv], k, &ctl->abort_flag)) {
             if (!ctl->abort_flag) record_error(a.err, BD_ERR_TIMEOUT);
             ctl->abort_flag = 1;
             break;
         }
-
-        float fv = 1.0f;   // MXFP4: 2^(reference exponent of this lane's V block)
+        const uint8_t* Vs = smem + (kNK + sv) * kMaxRec;
+        float op[8][4];   // MXFP4: this page's O, merged below with the page's V reference exponent
+        float fv = 1.0f;
         int ev_ref = 0;
         if (FMT == BD_FORMAT_MXFP4) {
+#pragma unroll
+            for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
             int em = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -586,57 +600,48 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            {
-                const uint32_t b01 = bfr[2 * i], b23 = bfr[2 * i + 1];
-                // dims 16g .. 16g+15 of pair rows t and t+4 sit at slot
-                // g ^ 2t: each quarter warp's eight 16-byte reads cover all
-                // 32 banks
-                const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * (g ^ (2 * t)));
-                const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * (g ^ (2 * t)));
-                uint32_t vs0, vs1;
-                if (FMT == BD_FORMAT_NVFP4) {
-                    vs0 = e4m3x2_to_f16x2(lds16(Vs + kCodeBytes + ((i * 8 + t) * 8 + g) * 2));
-                    vs1 = e4m3x2_to_f16x2(lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 8 + g) * 2));
-                } else {
-                    const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
-                    const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
-                    vs0 = f16_pow2((int)(e0 & 0xFF) - ev_ref) | (f16_pow2((int)(e0 >> 8) - ev_ref) << 16);
-                    vs1 = f16_pow2((int)(e1 & 0xFF) - ev_ref) | (f16_pow2((int)(e1 >> 8) - ev_ref) << 16);
-                }
-                const uint32_t vw0[4] = {v0.x, v0.y, v0.z, v0.w}, vw1[4] = {v1.x, v1.y, v1.z, v1.w};
+            // pair rows t and t + 4 of group i hold tokens 16i + 2t, +1 and
+            // 16i + 8 + 2t, +1 (k-slots 2t, 2t+1 and 2t+8, 2t+9); dims
+            // 16g .. 16g+15 sit at slot g ^ 2t: each quarter warp's eight
+            // 16-byte reads cover all 32 banks
+            const uint4 v0 = lds128(Vs + (i * 8 + t) * kD + 16 * (g ^ (2 * t)));
+            const uint4 v1 = lds128(Vs + (i * 8 + t + 4) * kD + 16 * (g ^ (2 * t)));
+            uint32_t vs0, vs1;
+            if (FMT == BD_FORMAT_NVFP4) {
+                vs0 = e4m3x2_to_f16x2(lds16(Vs + kCodeBytes + ((i * 8 + t) * 8 + g) * 2));
+                vs1 = e4m3x2_to_f16x2(lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 8 + g) * 2));
+            } else {
+                const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
+                const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
+                vs0 = f16_pow2((int)(e0 & 0xFF) - ev_ref) | (f16_pow2((int)(e0 >> 8) - ev_ref) << 16);
+                vs1 = f16_pow2((int)(e1 & 0xFF) - ev_ref) | (f16_pow2((int)(e1 >> 8) - ev_ref) << 16);
+            }
+            const uint32_t b01 = ph[2 * i], b23 = ph[2 * i + 1];
+            const uint32_t vw0[4] = {v0.x, v0.y, v0.z, v0.w}, vw1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // word j holds dims 16g+4j .. 16g+4j+3: m-tiles 2j (dims 4j, 4j+1) and 2j+1
-                    uint32_t f0[4], f1[4];
-                    e2m1x8_to_f16x2x4(vw0[j], f0);
-                    e2m1x8_to_f16x2x4(vw1[j], f1);
-                    uint32_t A[4];
-                    A[0] = hmul2(f0[0], vs0);
-                    A[1] = hmul2(f0[1], vs0);
-                    A[2] = hmul2(f1[0], vs1);
-                    A[3] = hmul2(f1[1], vs1);
-                    mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j] : op[2 * j], A, b01, b23);
-                    A[0] = hmul2(f0[2], vs0);
-                    A[1] = hmul2(f0[3], vs0);
-                    A[2] = hmul2(f1[2], vs1);
-                    A[3] = hmul2(f1[3], vs1);
-                    mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j + 1] : op[2 * j + 1], A, b01, b23);
-                }
+            for (int j = 0; j < 4; ++j) {
+                // word j holds dims 16g+4j .. 16g+4j+3: m-tiles 2j (dims 4j, 4j+1) and 2j+1
+                uint32_t f0[4], f1[4];
+                e2m1x8_to_f16x2x4(vw0[j], f0);
+                e2m1x8_to_f16x2x4(vw1[j], f1);
+                uint32_t A[4];
+                A[0] = hmul2(f0[0], vs0);
+                A[1] = hmul2(f0[1], vs0);
+                A[2] = hmul2(f1[0], vs1);
+                A[3] = hmul2(f1[1], vs1);
+                mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j] : op[2 * j], A, b01, b23);
+                A[0] = hmul2(f0[2], vs0);
+                A[1] = hmul2(f0[3], vs0);
+                A[2] = hmul2(f1[2], vs1);
+                A[3] = hmul2(f1[3], vs1);
+                mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j + 1] : op[2 * j + 1], A, b01, b23);
             }
         }
         // release the V slot: every lane's shared-memory reads are done
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyV[sv]));
-
-        // ---------------- merge the page into the warp's running state
-        lacc = fmaf(lacc, ex2(Mt - mnt), wpage * lpage);
-        Mt = mnt;
         if (FMT == BD_FORMAT_MXFP4) {
-            const float mnA = fmaxf(MA, mpA), mnB = fmaxf(MB, mpB);
-            const float aA = ex2(MA - mnA), aB = ex2(MB - mnB);
-            const float bA = ex2(mpA - mnA) * fv, bB = ex2(mpB - mnB) * fv;
-            MA = mnA;
-            MB = mnB;
+            const float bA = __shfl_sync(kFull, wpage, srcA) * fv, bB = __shfl_sync(kFull, wpage, srcB) * fv;
 #pragma unroll
             for (int bm = 0; bm < 8; ++bm) {
                 o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
@@ -648,31 +653,30 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, uint8_t*
     }
 
     // ---------------- hand the warp state to the CTA merge
-    __syncthreads();   // (A) all consumers are done with the ring
+    __syncthreads();   // (A) the ring and every MMA are done with
     float* sO = reinterpret_cast<float*>(smem);   // [consumer warps][4 heads][128]
     if (t < 2) {
 #pragma unroll
         for (int bm = 0; bm < 8; ++bm) {
             const int d = 16 * g + 2 * bm;
-            sO[(warp * 4 + 2 * t) * kD + d] = o[bm][0] * gV;
-            sO[(warp * 4 + 2 * t + 1) * kD + d] = o[bm][1] * gV;
-            sO[(warp * 4 + 2 * t) * kD + d + 1] = o[bm][2] * gV;
-            sO[(warp * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3] * gV;
+            sO[(w * 4 + 2 * t) * kD + d] = o[bm][0] * gV;
+            sO[(w * 4 + 2 * t + 1) * kD + d] = o[bm][1] * gV;
+            sO[(w * 4 + 2 * t) * kD + d + 1] = o[bm][2] * gV;
+            sO[(w * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3] * gV;
         }
     }
-    lacc += __shfl_xor_sync(kFull, lacc, 4);
-    lacc += __shfl_xor_sync(kFull, lacc, 8);
-    lacc += __shfl_xor_sync(kFull, lacc, 16);
-    if (g == 0) {
-        ctl->wm[warp][t] = Mt;
-        ctl->wl[warp][t] = lacc;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (t == 0 && g < 4) {
+        ctl->wm[w][g] = M;
+        ctl->wl[w][g] = l;
     }
 }
 
 // CTA merge of the states (consumer warps, then the BF16 tokens) into this
-// split's partial; a state with maximum -inf holds nothing and is skipped.
-__device__ void write_split_partial(const DecodeArgs& a, float* part, const uint8_t* smem, const Ctl* ctl) {
-    const int tid = threadIdx.x;
+// split's partial, by 128 threads tid = 0..127 (others pass tid >= 128); a
+// state with maximum -inf holds nothing and is skipped.
+__device__ void write_split_partial(const DecodeArgs& a, float* part, const uint8_t* smem, const Ctl* ctl, int tid) {
     if (tid >= 128) return;
     const int hh = tid >> 5, d0 = (tid & 31) * 4;
     const int nparts = a.nsplit + 1;
@@ -766,8 +770,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
 }
 
 template <int FMT, int PM>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {   // 128 registers
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeArgs a) {   // kLaunchRegs
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     // a negative length counts as 0; one past the block table's capacity keeps
     // its first max_blocks pages; both are argument errors
@@ -799,58 +803,76 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         }
         return;
     }
-    if (p0 >= p1) {
+    if (bf16) {
         // no FP4 pages: the consumer states are empty and nothing aborted
         if (threadIdx.x < kConsumers * 4) {
             ctl->wm[threadIdx.x >> 2][threadIdx.x & 3] = -INFINITY;
             ctl->wl[threadIdx.x >> 2][threadIdx.x & 3] = 0.0f;
         }
         if (threadIdx.x == 0) ctl->abort_flag = 0;
-    } else {
-        const int n = p1 - p0;
-        constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
-        if (threadIdx.x == 0) {
-            for (int s = 0; s < kNK; ++s) {
-                mbar_init(smem_u32(&ctl->fullK[s]), 1);
-                mbar_init(smem_u32(&ctl->emptyK[s]), 1);
-                ctl->tagK[s] = -1;
-                ctl->badK[s] = 0;
-            }
-            for (int s = 0; s < kNV; ++s) {
-                mbar_init(smem_u32(&ctl->fullV[s]), 1);
-                mbar_init(smem_u32(&ctl->emptyV[s]), 1);
-                ctl->tagV[s] = -1;
-            }
-            ctl->abort_flag = 0;
-            ctl->next_page = 0;
-            fence_mbar_init();
-        }
-        if (threadIdx.x < 128) {
-            // exact per-byte tables for the E4M3 scale byte bb: the correctly
-            // rounded 1/sd and the f16x2 pair (sd/c, sd/c) for the probability
-            // quantizer (exact: c is a power of two)
-            float* tab = reinterpret_cast<float*>(smem + kRingBytes + sizeof(Ctl));
-            const uint32_t bb = threadIdx.x;
-            const float sd = e4m3_value(bb);
-            const float cc = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
-            tab[bb] = (bb == 0) ? 0.0f : __frcp_rn(sd);
-            const uint32_t sdh = e4m3x2_to_f16x2(bb);
-            const uint32_t icc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / cc)));
-            reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
-        }
         __syncthreads();
-        if (warp >= kConsumers) {
-            // --------------------------------------------------- producers --
-            // warp 6 streams the pages' K records into the K ring, warp 7 their
-            // V records into the V ring, each in page order
-            const bool isK = (warp == kConsumers);
+        bf16_segment(a, b, h, L, smem, ctl);   // the same for the whole CTA
+        __syncthreads();
+        write_split_partial(a, part, smem, ctl, threadIdx.x);
+        return;
+    }
+
+    const int n = p1 - p0;
+    const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
+    constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
+    if (warp == 3) tmem_alloc(smem_u32(&ctl->tmem), kTmemCols);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNK; ++s) {
+            mbar_init(smem_u32(&ctl->fullK[s]), 1);
+            mbar_init(smem_u32(&ctl->emptyK[s]), 1);
+            ctl->tagK[s] = -1;
+        }
+        for (int s = 0; s < kNV; ++s) {
+            mbar_init(smem_u32(&ctl->fullV[s]), 1);
+            mbar_init(smem_u32(&ctl->emptyV[s]), 1);   // one consumer warp per page
+            ctl->tagV[s] = -1;
+        }
+        mbar_init(smem_u32(&ctl->accFull), 1);
+        mbar_init(smem_u32(&ctl->accEmpty), kConsumers);
+        for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&ctl->sfbFree[s]), 1);
+        mbar_init(smem_u32(&ctl->mmaDone), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x >= 128) {
+        // exact per-byte tables for the E4M3 scale byte bb: the correctly
+        // rounded 1/sd and the f16x2 pair (sd/c, sd/c) for the probability
+        // quantizer (exact: c is a power of two)
+        float* tab = reinterpret_cast<float*>(smem + kTabOff);
+        const uint32_t bb = threadIdx.x - 128;
+        const float sd = e4m3_value(bb);
+        const float cc = (float)((PM == BD_P_AMAX2_OR_AMAX6) ? a.p_c : 1);
+        tab[bb] = (bb == 0) ? 0.0f : __frcp_rn(sd);
+        const uint32_t sdh = e4m3x2_to_f16x2(bb);
+        const uint32_t icc = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(1.0f / cc)));
+        reinterpret_cast<uint32_t*>(tab)[128 + bb] = hmul2(bcast_lo(sdh), icc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // Each warpgroup keeps its own register share to the end: the control
+    // warpgroup gives registers back, the consumer warpgroup takes them, and
+    // the two branches never merge again (code after a merge would have to
+    // fit the smaller share).
+    static_assert(kCtlRegs == 40 && kConsumerRegs == 216, "the setmaxnreg immediates below");
+    if (warp < kFirstConsumer) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        if (warp < 2) {
+            // ----------------------------------------------------- producers --
+            // warp 0 streams the pages' K records into the K ring, warp 1
+            // their V records into the V ring, each in page order
+            const bool isK = (warp == 0);
             const int N = isK ? kNK : kNV;
             unsigned long long* fullb = isK ? ctl->fullK : ctl->fullV;
             unsigned long long* emptyb = isK ? ctl->emptyK : ctl->emptyV;
             int* tag = isK ? ctl->tagK : ctl->tagV;
             uint8_t* slots = smem + (isK ? 0 : kNK * kMaxRec);
             if (lane == 0) {
-                const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
                 // each page is read once per call: evict it from L2 first
                 const uint64_t policy = l2_evict_first_policy();
                 for (int k = 0; k < n; ++k) {
@@ -862,13 +884,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                         break;
                     }
                     const int64_t phys = bt[k];
-                    const bool ok = page_ok(phys, a.pool_pages);
                     const uint32_t full = smem_u32(&fullb[s]);
-                    if (isK) ctl->badK[s] = ok ? 0 : 1;   // published by the tag's release
-                    // tag the fill before it is armed: consumers accept a completed
-                    // phase only together with their own page index
+                    // tag the fill before it is armed: consumers accept a
+                    // completed phase only together with their own page index
                     st_release_shared(&tag[s], k);
-                    if (ok) {
+                    if (page_ok(phys, a.pool_pages)) {
                         const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
                         mbar_arrive_expect_tx(full, RB);
                         bulk_g2s_hint(smem_u32(slots + s * kMaxRec), rec, RB, full, policy);
@@ -880,26 +900,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
                 }
             }
             __syncthreads();   // (A)
-            // an aborted run drains the copies it left in flight before the ring
-            // is reused: a slot's last fill is the only one that can be pending
+            // an aborted run drains the copies it left in flight: a slot's last
+            // fill is the only one that can be pending
             if (lane == 0 && ctl->abort_flag) {
                 for (int s = 0; s < N; ++s) {
                     const int f = tag[s];
                     if (f >= 0) (void)mbar_wait_bounded(smem_u32(&fullb[s]), (f / N) & 1, kWaitLimitNs, nullptr);
                 }
             }
+        } else if (warp == 2) {
+            issue_qk<FMT>(a, b, h, n, bt, smem, ctl, lane);   // the MMA lane waits for its last MMA
+            __syncthreads();   // (A)
         } else {
-            consume_pages<FMT, PM>(a, b, h, n, smem, ctl, warp, lane);   // contains (A)
+            __syncthreads();   // (A): the consumers' last TMEM loads and every MMA are done
+            tc_fence_after();
+            tmem_dealloc(ctl->tmem, kTmemCols);
         }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+        const int q = warp - kFirstConsumer;
+        consume_pages<FMT, PM>(a, b, h, n, bt, smem, ctl, q, lane);   // contains (A)
+        if (q == 0 && lane < 4) {   // no BF16 tokens in an FP4 split
+            ctl->wm[kConsumers][lane] = -INFINITY;
+            ctl->wl[kConsumers][lane] = 0.0f;
+        }
+        named_bar_sync(1, kConsumers * 32);   // (B) the four warp states are in shared memory
+        write_split_partial(a, part, smem, ctl, threadIdx.x - kFirstConsumer * 32);
     }
-    if (!bf16 && threadIdx.x < 4) {
-        ctl->wm[kConsumers][threadIdx.x] = -INFINITY;
-        ctl->wl[kConsumers][threadIdx.x] = 0.0f;
-    }
-    __syncthreads();   // (B) warp states and drained ring
-    if (bf16) bf16_segment(a, b, h, L, smem, ctl);   // the same for the whole CTA
-    __syncthreads();
-    write_split_partial(a, part, smem, ctl);
 }
 
 // ------------------------------------------------------ bounded-wait test --
@@ -951,9 +978,9 @@ int device_sms() {
 
 void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split) {
     const int sms = device_sms();
-    // two CTAs fit per SM; split 0 of every (sequence, kv head) is the BF16
-    // sink/tail CTA, so a single wave holds units * (splits + 1) CTAs
-    const int slots = 2 * sms;
+    // kCtasPerSm CTAs fit per SM; split 0 of every (sequence, kv head) is the
+    // BF16 sink/tail CTA, so a single wave holds units * (splits + 1) CTAs
+    const int slots = kCtasPerSm * sms;
     const int units = max(1, B * hkv);
     int ns = max(1, slots / units - 1);
     ns = max(1, min(ns, max(1, max_blocks)));
@@ -994,7 +1021,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
         if (dev < 0) return cudaErrorInvalidDevice;
         std::lock_guard<std::mutex> g(g_dev_lock);
         if (!g_dev[dev].smem_attr[f][pm]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            // the register split inside the kernel assumes this launch allocation
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
             g_dev[dev].smem_attr[f][pm] = true;
         }

@@ -15,7 +15,7 @@
 //    Hadamard transform runs strides 1..8 inside a lane and strides 16, 32,
 //    64 across lanes c^1, c^2, c^4 by warp shuffles; an NVFP4 block (16 dims)
 //    is then entirely in one lane, an MXFP4 block (32 dims) in a lane pair.
-//  V warp: lane = (token pair p = lane%8: tokens 16i+p and 16i+p+8, 32-dim
+//  V warp: lane = (token pair p = lane%8: tokens 16i+2p and 16i+2p+1, 32-dim
 //    chunk c = lane/8), so both nibbles of a V code byte are produced in the
 //    same lane and the 16-token tile is written with 16-byte stores.
 // Every rounding step is the IEEE binary32 operation the oracle performs
@@ -236,9 +236,13 @@ __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, int row0,
             enc16<false>(x, 0.0f, down, amax32 == 0.0f, w0, w1, w);
             sb = (amax32 == 0.0f) ? 0u : (uint32_t)(e + 127);
         }
-        *reinterpret_cast<uint2*>(rec + tok * 64 + 8 * c) = make_uint2(w0, w1);
-        if (FMT == BD_FORMAT_NVFP4) rec[kCodeBytes + tok * 8 + c] = (uint8_t)sb;
-        else if (!(c & 1)) rec[kCodeBytes + tok * 4 + (c >> 1)] = (uint8_t)sb;
+        // codes in groups of 8 tokens x 32 dims (128 B each); scale byte of
+        // block b at (b/4)*512 + (tok%32)*16 + (tok/32)*4 + b%4
+        *reinterpret_cast<uint2*>(rec + (tok >> 3) * 512 + (c >> 1) * 128 + (tok & 7) * 16 + 8 * (c & 1)) =
+            make_uint2(w0, w1);
+        const int sline = kCodeBytes + (tok & 31) * 16 + (tok >> 5) * 4;
+        if (FMT == BD_FORMAT_NVFP4) rec[sline + (c >> 2) * 512 + (c & 3)] = (uint8_t)sb;
+        else if (!(c & 1)) rec[sline + (c >> 1)] = (uint8_t)sb;
     }
 }
 
@@ -284,7 +288,7 @@ template <int FMT>
 __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, int row0, const float* stab, uint8_t* rec,
                              int grp, int lane) {
     const int p = lane & 7, c = lane >> 3;
-    const int t0 = 16 * grp + p, t1 = t0 + 8;
+    const int t0 = 16 * grp + 2 * p, t1 = t0 + 1;
     const uint8_t* r0 = tile + (t0 - row0) * kTilePitch + 64 * c;   // dims 32c .. 32c+31 of both tokens
     const uint8_t* r1 = tile + (t1 - row0) * kTilePitch + 64 * c;
     // dims 32c .. 32c+31 are 16-byte slots 2c, 2c+1, stored at slots

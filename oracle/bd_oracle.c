@@ -310,17 +310,28 @@ static int64_t rec_off(const or_config* c, int64_t page, int h, int kv) {
     return ((page * c->num_kv_heads + h) * 2 + kv) * or_record_bytes(c);
 }
 
-/* K record: codes[tok][64] (dim d in byte d/2, even d in the low nibble),
- * then scales[tok][nb] (block b of the token's head vector). */
-static void put_k(const or_config* c, uint8_t* rec, int tok, const uint8_t* codes128, const uint8_t* sbs) {
-    for (int d = 0; d < OR_D; d += 2)
-        rec[tok * 64 + d / 2] = (uint8_t)((codes128[d] & 0xF) | ((codes128[d + 1] & 0xF) << 4));
-    for (int b = 0; b < nblk(c); b++) rec[OR_CODE_BYTES + tok * nblk(c) + b] = sbs[b];
+/* K record.  Codes: the byte of dims d, d+1 (d even; d in the low nibble)
+ * of token t sits at (t/8)*512 + (d/32)*128 + (t%8)*16 + (d%32)/2, i.e. in
+ * groups of 8 tokens x 32 dims, each group 128 contiguous bytes.  Scales: the
+ * byte of block b of token t sits at 8192 + (b/4)*512 + (t%32)*16 + (t/32)*4
+ * + b%4 (512-byte groups of 32 lines of 16 bytes; line i holds tokens i,
+ * i+32, i+64, i+96, four blocks each). */
+static int64_t k_code_off(int tok, int d) {
+    return (int64_t)(tok / 8) * 512 + (d / 32) * 128 + (tok % 8) * 16 + (d % 32) / 2;
+}
+static int64_t k_scale_off(int tok, int b) {
+    return OR_CODE_BYTES + (int64_t)(b / 4) * 512 + (tok % 32) * 16 + (tok / 32) * 4 + b % 4;
 }
 
-/* V record: tokens are paired (tau, tau+8) inside each 16-token group i
- * (tau = 16 i + p, p = 0..7).  Row (i, p) is 128 bytes: the byte of head
- * dim d holds token tau in the low nibble and token tau+8 in the high
+static void put_k(const or_config* c, uint8_t* rec, int tok, const uint8_t* codes128, const uint8_t* sbs) {
+    for (int d = 0; d < OR_D; d += 2)
+        rec[k_code_off(tok, d)] = (uint8_t)((codes128[d] & 0xF) | ((codes128[d + 1] & 0xF) << 4));
+    for (int b = 0; b < nblk(c); b++) rec[k_scale_off(tok, b)] = sbs[b];
+}
+
+/* V record: tokens are paired (tau, tau+1) inside each 16-token group i
+ * (tau = 16 i + 2 p, p = 0..7).  Row (i, p) is 128 bytes: the byte of head
+ * dim d holds token tau in the low nibble and token tau+1 in the high
  * nibble, and the 16 bytes of dims 16c..16c+15 sit at 16-byte slot
  * c XOR 2(p mod 4) of the row.  scales[i][p][b][2] holds the two tokens'
  * scale bytes of block b, token tau first. */
@@ -329,7 +340,7 @@ static int v_code_off(int i, int p, int d) {
 }
 
 static void put_v(const or_config* c, uint8_t* rec, int tok, const uint8_t* codes128, const uint8_t* sbs) {
-    int i = tok / 16, r = tok % 16, p = r % 8, hi = r / 8;
+    int i = tok / 16, r = tok % 16, p = r / 2, hi = r % 2;
     for (int d = 0; d < OR_D; d++) {
         uint8_t* byte = &rec[v_code_off(i, p, d)];
         if (hi) *byte = (uint8_t)((*byte & 0x0F) | ((codes128[d] & 0xF) << 4));
@@ -339,19 +350,20 @@ static void put_v(const or_config* c, uint8_t* rec, int tok, const uint8_t* code
 }
 
 static uint8_t get_k_code(const uint8_t* rec, int tok, int d) {
-    uint8_t byte = rec[tok * 64 + d / 2];
+    uint8_t byte = rec[k_code_off(tok, d & ~1)];
     return (d & 1) ? (byte >> 4) : (byte & 0xF);
 }
 static uint8_t get_k_scale(const or_config* c, const uint8_t* rec, int tok, int b) {
-    return rec[OR_CODE_BYTES + tok * nblk(c) + b];
+    (void)c;
+    return rec[k_scale_off(tok, b)];
 }
 static uint8_t get_v_code(const uint8_t* rec, int tok, int d) {
-    int i = tok / 16, r = tok % 16, p = r % 8, hi = r / 8;
+    int i = tok / 16, r = tok % 16, p = r / 2, hi = r % 2;
     uint8_t byte = rec[v_code_off(i, p, d)];
     return hi ? (byte >> 4) : (byte & 0xF);
 }
 static uint8_t get_v_scale(const or_config* c, const uint8_t* rec, int tok, int b) {
-    int i = tok / 16, r = tok % 16, p = r % 8, hi = r / 8;
+    int i = tok / 16, r = tok % 16, p = r / 2, hi = r % 2;
     return rec[OR_CODE_BYTES + ((i * 8 + p) * nblk(c) + b) * 2 + hi];
 }
 

@@ -1,11 +1,13 @@
 """Test-side reader of the packed byte layouts (written independently of the
 oracle and of the CUDA path, from the layout the public header documents).
 
-K record (per page, KV head): codes[128 tok][64 B] (head-dim element d in
-byte d/2, even d in the low nibble), then scales[128 tok][nb].
+K record (per page, KV head): codes in groups of 8 tokens x 32 dims: the
+byte of dims d, d+1 (even d in the low nibble) of token t is at
+(t//8)*512 + (d//32)*128 + (t%8)*16 + (d%32)//2; then the scales: block b of
+token t at 8192 + (b//4)*512 + (t%32)*16 + (t//32)*4 + b%4.
 V record: codes[8 groups][8 pairs][8 slots][16 B]; the byte of head dim d
-holds token 16i+p (low nibble) and token 16i+p+8 (high nibble) and sits at
-slot (d // 16) ^ 2 (p % 4), byte d % 16; scales[8][8][nb][2] (token 16i+p
+holds token 16i+2p (low nibble) and token 16i+2p+1 (high nibble) and sits at
+slot (d // 16) ^ 2 (p % 4), byte d % 16; scales[8][8][nb][2] (token 16i+2p
 first).
 nb = 8 E4M3 bytes (NVFP4, 16-element blocks) or 4 UE8M0 bytes (MXFP4, 32).
 Pool: records ordered [page][kv_head][K, V].
@@ -47,11 +49,14 @@ def scale_values(fmt: int, sbytes: np.ndarray) -> np.ndarray:
 def k_record(fmt: int, rec: np.ndarray):
     """-> (codes [128][128] uint8, scale bytes [128][nb], values [128][128] fp64 without g)."""
     nb = nblocks(fmt)
-    by = rec[:8192].reshape(128, 64)
+    # [t//8][d//32][t%8][(d%32)//2] -> [t][d//2]
+    by = rec[:8192].reshape(16, 4, 8, 16).transpose(0, 2, 1, 3).reshape(128, 64)
     codes = np.empty((128, 128), np.uint8)
     codes[:, 0::2] = by & 0xF
     codes[:, 1::2] = by >> 4
-    sb = rec[8192:8192 + 128 * nb].reshape(128, nb)
+    t = np.arange(128)[:, None]
+    b = np.arange(nb)[None, :]
+    sb = rec[8192 + (b // 4) * 512 + (t % 32) * 16 + (t // 32) * 4 + b % 4]
     vals = E2M1[codes] * np.repeat(scale_values(fmt, sb), 128 // nb, axis=1)
     return codes, sb, vals
 
@@ -69,10 +74,10 @@ def v_record(fmt: int, rec: np.ndarray):
     sb = np.empty((128, nb), np.uint8)
     for i in range(8):
         for p in range(8):
-            codes[16 * i + p] = by[i, p] & 0xF
-            codes[16 * i + p + 8] = by[i, p] >> 4
-            sb[16 * i + p] = sbr[i, p, :, 0]
-            sb[16 * i + p + 8] = sbr[i, p, :, 1]
+            codes[16 * i + 2 * p] = by[i, p] & 0xF
+            codes[16 * i + 2 * p + 1] = by[i, p] >> 4
+            sb[16 * i + 2 * p] = sbr[i, p, :, 0]
+            sb[16 * i + 2 * p + 1] = sbr[i, p, :, 1]
     vals = E2M1[codes] * np.repeat(scale_values(fmt, sb), 128 // nb, axis=1)
     return codes, sb, vals
 
