@@ -215,7 +215,8 @@ int bd_append_kv(bd_ctx* ctx, int layer, const void* k_new, const void* v_new, c
                  void* tail_v, int B, float k_gscale, float v_gscale, void* kv_pool, void* stream);
 
 /* Workspace bytes bd_decode_attention needs for B sequences whose block
- * table rows hold max_blocks entries (0 if B == 0). */
+ * table rows hold max_blocks entries (0 if B == 0): the split partials and
+ * one 8-byte arrival counter per (sequence, kv head). */
 size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
 
 /* Paged single-token decode attention over the hybrid cache ([arch] decode
@@ -242,16 +243,18 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *   k/v_gscale  : the per-tensor scales the layer's pages were written with.
  *   out         : fp32 [B][num_q_heads][128], device.
  *   ws          : device scratch of at least bd_decode_workspace_size(ctx, B,
- *                 max_blocks) bytes for the split partials; it needs no
- *                 initialization.  Calls that share a workspace must not
- *                 overlap on the GPU.
+ *                 max_blocks) bytes for the split partials and the split
+ *                 arrival counters; it needs no initialization (a counter
+ *                 carries a per-call tag: bytes from earlier calls or never
+ *                 written count as zero).  Calls that share a workspace must
+ *                 not overlap on the GPU.
  * Query head j reads kv head j / 4; softmax scale 1/sqrt(128).
- * Two kernels are launched on `stream`: the split decode, then the split
- * combine, which starts under programmatic dependent launch and reads the
- * partials once the decode grid has completed.
+ * One kernel is launched on `stream`: each split writes its partial to ws
+ * and counts itself in at its (sequence, kv head)'s counter, and the split
+ * that completes the count merges that group's partials into out.
  * Ordering: the kernel may start reading kv_pool, block_table and seq_lens
  * while the preceding grid in the stream, if it allows programmatic early
- * launch, still runs (this library's query, decode and combine kernels do); those
+ * launch, still runs (this library's query and decode kernels do); those
  * inputs must be written by work that completes before that grid starts
  * (bd_quantize_kv_pages and bd_append_kv never allow early launch).  q_packed, q, the sink and
  * tail rows, out and ws are touched only after the preceding grid has
@@ -271,16 +274,16 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
  * front -- and so cannot provide the workspace bd_decode_attention needs.
  * Arguments are those of bd_decode_attention minus ws / ws_bytes; inputs and
  * out are still caller-owned device memory.
- *  - The split partials live in one fixed 4 MiB device array inside the
- *    library (every GPU that loads the library holds it until the process
- *    exits).  A call whose partials need more
+ *  - The split partials and arrival counters live in one fixed 4 MiB device
+ *    array inside the library (every GPU that loads the library holds it
+ *    until the process exits).  A call whose workspace would need more
  *    (bd_decode_workspace_size(ctx, B, max_blocks) > 4 MiB) is rejected with
  *    BD_ERR_WORKSPACE before anything is launched: use bd_decode_attention
  *    with a workspace instead.
  *  - Nothing in that array has to start at zero: each call writes every
- *    partial it reads.  Every call shares the array, so calls that overlap
- *    on the GPU (other streams, other threads) race and must be serialized
- *    by the caller.
+ *    partial it reads, and its counters carry the call's own tag.  Every
+ *    call shares the array, so calls that overlap on the GPU (other
+ *    streams, other threads) race and must be serialized by the caller.
  *  - The first call on a device looks up the array's device address; make
  *    that first call before capturing a stream into a CUDA graph.
  *  - Like every launch call it must run on the context's device (the device

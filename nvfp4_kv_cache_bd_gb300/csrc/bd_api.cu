@@ -213,7 +213,7 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks) {
     if (!ctx || B <= 0 || max_blocks < 0) return 0;
     int ns = 0, pps = 0;
     bd::decode_splits(B, ctx->cfg.num_kv_heads, max_blocks, &ns, &pps);
-    return bd::decode_ws_bytes(B, ctx->cfg.num_q_heads, ns);
+    return bd::decode_ws_bytes(B, ctx->cfg.num_q_heads, ctx->cfg.num_kv_heads, ns);
 }
 
 int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void* q, const void* kv_pool,
@@ -254,6 +254,9 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     a.hkv = ctx->cfg.num_kv_heads;
     a.max_blocks = max_blocks;
     bd::decode_splits(B, a.hkv, max_blocks, &a.nsplit, &a.pages_per_split);
+    a.counters = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) +
+                                                       bd::decode_parts_bytes(B, a.hq, a.nsplit));
+    a.tag = bd::next_decode_tag();
     a.pool_pages = ctx->cfg.pool_pages;
     a.format = ctx->cfg.format;
     a.centering = ctx->cfg.centering;
@@ -316,6 +319,9 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     a.hkv = ctx->cfg.num_kv_heads;
     a.max_blocks = max_blocks;
     bd::decode_splits(B, a.hkv, max_blocks, &a.nsplit, &a.pages_per_split);
+    a.counters = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(scratch) +
+                                                       bd::decode_parts_bytes(B, a.hq, a.nsplit));
+    a.tag = bd::next_decode_tag();
     a.pool_pages = ctx->cfg.pool_pages;
     a.format = ctx->cfg.format;
     a.centering = ctx->cfg.centering;

@@ -1,6 +1,6 @@
 // Paged single-token decode attention over the hybrid cache (BF16 sink +
-// packed FP4 pages + BF16 tail): flash-decoding split-K over pages, then a
-// separate kernel that merges the splits.
+// packed FP4 pages + BF16 tail): flash-decoding split-K over pages, the
+// splits merged by the last split of each (sequence, kv head) to finish.
 //
 // Method: "How openbitsys/bitdecoding-fp4 works" (decode interface -> paged
 // attention kernel; hybrid cache); BitDecoding-FP4 evaluation config
@@ -8,14 +8,13 @@
 // probability_environment ("amax6" / "amax2_or_amax6" with c in {1, 8} and
 // tau in [0, 448]), RECIPE dual_residual_query_quantization (two query terms).
 //
-// Grid (nsplit + 1, kv heads, sequences) of 256-thread CTAs, two per SM.
-// Split 0 of a (sequence, kv head) attends the BF16 sink and tail tokens with
-// exact probabilities; split s >= 1 takes that sequence's FP4 pages
-// [(s - 1) * pages_per_split, s * pages_per_split).  The split-0 CTAs are
-// short: the SM slots they free early in a layer let the split combine and
-// the next layer's query and decode kernels become resident before this
-// decode ends, so the next decode's producers fill their rings during this
-// one's tail.
+// Grid (nsplit + 1, kv heads, sequences) of 256-thread CTAs, two per SM; a
+// single-wave grid leaves a few SM slots free for the next layer's query
+// quantizer.  Split 0 of a (sequence, kv head) attends the BF16 sink and tail
+// tokens with exact probabilities; split s >= 1 takes that sequence's FP4
+// pages [(s - 1) * pages_per_split, s * pages_per_split).  As this layer's
+// CTAs finish, the next layer's decode CTAs take their slots, so the next
+// decode's producers fill their rings during this one's tail.
 //
 // FP4 split CTA, two warpgroups with their own register shares:
 //  warp 0    streams the pages' K records, in page order, into a 4-slot
@@ -45,16 +44,22 @@
 //            query head; their results are never read.
 // Every page's K and V record is read once from HBM; each page is processed
 // by one warp in a fixed order, so a split's result does not depend on
-// scheduling.  combine_kernel, one CTA per (sequence, query head), merges the
-// splits: O = sum 2^(m-M) O / sum 2^(m-M) l.
+// scheduling.  Each split writes its partial (m, l, O per query head) to the
+// workspace and counts itself in at its (sequence, kv head)'s arrival
+// counter; the split that completes the count merges that group's partials,
+// O = sum 2^(m-M) O / sum 2^(m-M) l, in a fixed split order, so the result
+// does not depend on which split came last either.  With no separate merge
+// kernel, a layer is one grid: nothing of a layer's chain holds an SM slot
+// the next layer's decode CTAs could use.
 //
-// The query, decode and combine kernels use programmatic dependent launch:
-// the producers start streaming pages while the query quantizer still runs;
+// The query and decode kernels use programmatic dependent launch: the
+// producers start streaming pages while the query quantizer still runs;
 // every thread that reads the packed or raw query or the sink/tail rows, or
 // writes the workspace or out, first waits on the preceding grid.
 #include <math.h>
 #include <stddef.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "bd_device.cuh"
@@ -80,16 +85,17 @@ static_assert(kCtlRegs % 8 == 0 && kConsumerRegs % 8 == 0 && kConsumerRegs <= 25
 constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
 constexpr int kWavePages = 32;   // one-wave splits up to this many pages ...
 constexpr int kBatchPages = 16;  // ... else splits of this many (more if kMaxSplits needs it)
-constexpr int kMaxSplits = 64;    // splits + 1 per (sequence, kv head); the combine stages them in 33.8 KB
+constexpr int kMaxSplits = 64;    // splits + 1 per (sequence, kv head)
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
 // Tensor memory of an FP4 split CTA (256 columns): the score buffer at
 // columns 0..127 (one column per token of the page), the query's scale
-// factors at 128 (+16 for the second NVFP4 group), and two slots of a page's
-// K scale factors at 160 + 32 s (+16).  Every scale-factor address starts on
-// a 16-column boundary.
+// factors at 128 (+16 for the second NVFP4 group), and three slots of a
+// page's K scale factors at 160 + 32 s (+16).  Every scale-factor address
+// starts on a 16-column boundary.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSfaCol = 128;
+constexpr int kSfbSlots = 3;
 __device__ __forceinline__ uint32_t sfb_col(int slot, int j) { return 160u + 32u * slot + 16u * j; }
 constexpr int kN = 128;                          // MMA N: the page's tokens
 // The query operand: 28 core-matrix groups of 8 rows x 64 B, all zero but
@@ -103,11 +109,13 @@ struct alignas(16) Ctl {
     unsigned long long fullV[kNV], emptyV[kNV];   // V ring (empty: the page's consumer warp)
     unsigned long long accFull;                   // a round's scores are in the buffer
     unsigned long long accEmpty;                  // all four consumer warps have read the round
-    unsigned long long sfbFree[2];                // a K scale-factor slot's MMAs completed
+    unsigned long long sfbFree[kSfbSlots];                // a K scale-factor slot's MMAs completed
     unsigned long long mmaDone;                   // every MMA the CTA issued has completed
+    unsigned long long mergeBar;                  // the merging split's staged partials arrived
     float wm[kConsumers + 1][4];   // per-warp running max per head (log2 units); last: BF16 tokens
     float wl[kConsumers + 1][4];   // per-warp softmax denominator per head
     int abort_flag;
+    int last_split;                // this split completed its group's arrival count
     int tagK[kNK], tagV[kNV];      // page index each slot's latest fill holds (-1: none)
     uint32_t tmem;                 // TMEM base address
 };
@@ -332,14 +340,14 @@ __device__ void mma_rounds(const DecodeArgs& a, int n, const int32_t* bt, uint8_
         for (int w = 0; w < 4; ++w) {
             const int k = 4 * r + w;
             if (k >= n) break;
-            const int s = k % kNK, slot = k & 1;
+            const int s = k % kNK, slot = k % kSfbSlots;
             if (!wait_stage_page(smem_u32(&ctl->fullK[s]), (k / kNK) & 1, &ctl->tagK[s], k, &ctl->abort_flag)) {
                 aborted = true;
                 break;
             }
-            // the scale-factor slot's previous MMAs (page k - 2) have completed
-            if (k >= 2 && !mbar_wait_bounded(smem_u32(&ctl->sfbFree[slot]), ((k >> 1) - 1) & 1, kWaitLimitNs,
-                                             &ctl->abort_flag)) {
+            // the scale-factor slot's previous MMAs (page k - kSfbSlots) have completed
+            if (k >= kSfbSlots && !mbar_wait_bounded(smem_u32(&ctl->sfbFree[slot]), ((k / kSfbSlots) - 1) & 1,
+                                                     kWaitLimitNs, &ctl->abort_flag)) {
                 aborted = true;
                 break;
             }
@@ -558,7 +566,7 @@ __device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, const in
                 bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
                 bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
                 const bool two = (PM == BD_P_AMAX2_OR_AMAX6) && (bm < tau);
-                const uint32_t sb = e4m3(two ? bm * 0.5f : div6(bm));
+                const uint32_t sb = two ? e4m3(bm * 0.5f) : e4m3_div6(bm);
                 const float inv = ptab_rcp[sb];   // 0 for the zero scale: all codes 0
                 const uint32_t sdc = ptab_sdc[sb];
                 ph[2 * i] = hmul2(e2m1x2_to_f16x2(e2m1x2(__fmul_rn(u[0], inv), __fmul_rn(u[1], inv))), sdc);
@@ -706,67 +714,126 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
     }
 }
 
-// Merge the split partials of (sequence b, query head j) into out: one CTA
-// of 128 threads per (b, j), launched after the decode with programmatic
-// dependent launch.  The head's partials (one contiguous block of
-// nsplit + 1 records) are staged into shared memory with 16-byte
-// asynchronous copies; warp 0 finds the maximum M over the splits (one
-// integer warp reduction of order-preserving keys), the weights
-// w_s = 2^(m_s - M) (0 for an empty split) and the denominator sum w_s l_s;
-// thread d then sums w_s O_s[d].
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
-    __shared__ __align__(16) float sp[kMaxSplits * kPartStride];
-    __shared__ float sw[kMaxSplits];
-    __shared__ float sden;
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int bj = blockIdx.x;   // b * hq + j
-    const int nparts = a.nsplit + 1;   // partials per (sequence, query head)
-    const int tid = threadIdx.x, lane = tid & 31;
-    const float* base = a.parts + (size_t)bj * nparts * kPartStride;
-    griddep_wait();   // the decode grid has completed: its partials are visible
-    for (int i = tid; i < nparts * (kPartStride / 4); i += blockDim.x) cp_async16(smem_u32(sp + 4 * i), base + 4 * i);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (tid < 32) {
-        float m[2], l[2];
-        uint32_t key = 0;   // order-preserving u32 key of the largest m with l > 0
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int sidx = lane + 32 * r;
-            m[r] = (sidx < nparts) ? sp[sidx * kPartStride] : -INFINITY;
-            l[r] = (sidx < nparts) ? sp[sidx * kPartStride + 1] : 0.0f;
-            if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
-        }
-        key = __reduce_max_sync(kFull, key);
-        const float M = (key == 0) ? -INFINITY : f32_from_order_key(key);
-        float den = 0.0f;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int sidx = lane + 32 * r;
-            const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
-            if (sidx < nparts) sw[sidx] = w;
-            den = fmaf(w, l[r], den);
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
-        if (lane == 0) sden = den;
+// Count this split in at its (sequence, kv head) group's arrival counter and
+// report whether it completed the count.  The counter word holds the call's
+// 40-bit tag over a 24-bit count.  A word with another tag (an earlier
+// call's, or workspace bytes never written) is first re-tagged with count 0
+// by one compare-and-swap -- it fails only if another split of this call got
+// there first, and every later update keeps this call's tag -- and then each
+// split adds 1 with one atomic add, which the L2 serves without retries.
+__device__ bool count_split_in(const DecodeArgs& a, int b, int h) {
+    unsigned long long* cnt = a.counters + (size_t)b * a.hkv + h;
+    const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(cnt);
+    if ((w >> 24) != a.tag) atomicCAS(cnt, w, a.tag << 24);
+    const unsigned long long old = atomicAdd(cnt, 1ull);
+    return (old & 0xFFFFFFull) == (unsigned long long)a.nsplit;   // nsplit + 1 arrivals in all
+}
+
+// Merge the nsplit + 1 partials of query heads 4h .. 4h+3 of sequence b into
+// out, by 128 threads tid = 0..127 synchronised on named barrier 1.  G heads
+// at a time (4 when their records fit the ring area, else 2) are staged into
+// shared memory by one bulk asynchronous copy (the TMA unit reads L2, where
+// the other SMs' partials are); warp hh finds head hh's maximum M over the
+// splits with l > 0 (one integer warp reduction of order-preserving keys), the
+// weights w_s = 2^(m_s - M) and the denominator sum w_s l_s; each thread then
+// sums w_s O_s over its G output dims in split order.  A split with w_s = 0
+// wrote no O (its bytes may hold anything, NaN included): it is skipped.
+__device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ctl* ctl, int tid) {
+    const int nparts = a.nsplit + 1;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int G = (4 * nparts * kPartStride * 4 <= kRingBytes - 4 * 4 * (kMaxSplits + 1)) ? 4 : 2;
+    float* stage = reinterpret_cast<float*>(smem);
+    float* sw = stage + G * nparts * kPartStride;   // [G][kMaxSplits] weights, then [G] denominators
+    float* sden = sw + G * kMaxSplits;
+    const uint32_t bar = smem_u32(&ctl->mergeBar);
+    const uint32_t bytes = (uint32_t)(G * nparts * kPartStride * 4);   // a multiple of 16
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
     }
-    __syncthreads();
-    const float* ph = sp + 4 + tid;
-    float n0 = 0.0f, n1 = 0.0f;
-    int sidx = 0;
-#pragma unroll 4
-    // an empty split wrote no O (its workspace bytes may hold anything, NaN
-    // included): it is skipped, not multiplied by its zero weight
-    for (; sidx + 1 < nparts; sidx += 2) {
-        const float w0 = sw[sidx], w1 = sw[sidx + 1];
-        if (w0 != 0.0f) n0 = fmaf(w0, ph[sidx * kPartStride], n0);
-        if (w1 != 0.0f) n1 = fmaf(w1, ph[(sidx + 1) * kPartStride], n1);
+    // this thread's earlier shared-memory accesses come before the copy's writes
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    for (int h0 = 0, pass = 0; h0 < 4; h0 += G, ++pass) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(smem_u32(stage), a.parts + (size_t)(b * a.hq + 4 * h + h0) * nparts * kPartStride, bytes, bar);
+        }
+        if (!mbar_wait_bounded(bar, pass & 1, kWaitLimitNs, nullptr)) {
+            if (tid == 0) record_error(a.err, BD_ERR_TIMEOUT);
+            return;   // every thread gives up at the same wait
+        }
+        if (warp < G) {
+            const float* hp = stage + warp * nparts * kPartStride;
+            float m[2], l[2];
+            uint32_t key = 0;   // order-preserving key of the largest m with l > 0
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int sidx = lane + 32 * r;
+                m[r] = (sidx < nparts) ? hp[sidx * kPartStride] : -INFINITY;
+                l[r] = (sidx < nparts) ? hp[sidx * kPartStride + 1] : 0.0f;
+                if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
+            }
+            key = __reduce_max_sync(kFull, key);
+            const float M = (key == 0) ? -INFINITY : f32_from_order_key(key);
+            float den = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int sidx = lane + 32 * r;
+                const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
+                if (sidx < nparts) sw[warp * kMaxSplits + sidx] = w;
+                den = fmaf(w, l[r], den);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
+            if (lane == 0) sden[warp] = den;
+        }
+        named_bar_sync(1, 128);
+        // thread tid: head h0 + tid / (128 / G), G consecutive dims
+        const int hh = tid / (128 / G), d0 = (tid % (128 / G)) * G;
+        const float* hp = stage + hh * nparts * kPartStride + 4 + d0;
+        const float* w = sw + hh * kMaxSplits;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sidx = 0; sidx < nparts; ++sidx) {
+            const float ws = w[sidx];
+            if (ws == 0.0f) continue;
+            if (G == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(hp + sidx * kPartStride);
+                acc[0] = fmaf(ws, v.x, acc[0]);
+                acc[1] = fmaf(ws, v.y, acc[1]);
+                acc[2] = fmaf(ws, v.z, acc[2]);
+                acc[3] = fmaf(ws, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(hp + sidx * kPartStride);
+                acc[0] = fmaf(ws, v.x, acc[0]);
+                acc[1] = fmaf(ws, v.y, acc[1]);
+            }
+        }
+        const float den = sden[hh];
+        const float inv = (den > 0.0f) ? 1.0f / den : 0.0f;
+        float* o = a.out + ((size_t)b * a.hq + 4 * h + h0 + hh) * kD + d0;
+        if (G == 4) {
+            *reinterpret_cast<float4*>(o) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+        } else {
+            *reinterpret_cast<float2*>(o) = make_float2(acc[0] * inv, acc[1] * inv);
+        }
+        // the staging area is rewritten by the next pass's copy
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
     }
-    if (sidx < nparts && sw[sidx] != 0.0f) n0 = fmaf(sw[sidx], ph[sidx * kPartStride], n0);
-    const float den = sden;
-    a.out[(size_t)bj * kD + tid] = (den > 0.0f) ? (n0 + n1) * (1.0f / den) : 0.0f;
+}
+
+// End of a split, by 128 threads tid = 0..127 (named barrier 1) once each has
+// written its share of the split's partial: count the split in and, if it
+// was the last of its group, merge the group.
+__device__ void finish_split(const DecodeArgs& a, int b, int h, uint8_t* smem, Ctl* ctl, int tid) {
+    __threadfence();   // this thread's partial writes are visible device-wide before the count
+    named_bar_sync(1, 128);
+    if (tid == 0) ctl->last_split = count_split_in(a, b, h) ? 1 : 0;
+    named_bar_sync(1, 128);
+    if (!*reinterpret_cast<volatile int*>(&ctl->last_split)) return;
+    __threadfence();   // the other splits' partials, counted in before this one
+    merge_group(a, b, h, smem, ctl, tid);
 }
 
 template <int FMT, int PM>
@@ -801,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
             part[threadIdx.x * (a.nsplit + 1) * kPartStride + 0] = -INFINITY;
             part[threadIdx.x * (a.nsplit + 1) * kPartStride + 1] = 0.0f;
         }
+        if (threadIdx.x < 128) finish_split(a, b, h, smem, ctl, threadIdx.x);
         return;
     }
     if (bf16) {
@@ -814,6 +882,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         bf16_segment(a, b, h, L, smem, ctl);   // the same for the whole CTA
         __syncthreads();
         write_split_partial(a, part, smem, ctl, threadIdx.x);
+        if (threadIdx.x < 128) finish_split(a, b, h, smem, ctl, threadIdx.x);
         return;
     }
 
@@ -834,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         }
         mbar_init(smem_u32(&ctl->accFull), 1);
         mbar_init(smem_u32(&ctl->accEmpty), kConsumers);
-        for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&ctl->sfbFree[s]), 1);
+        for (int s = 0; s < kSfbSlots; ++s) mbar_init(smem_u32(&ctl->sfbFree[s]), 1);
         mbar_init(smem_u32(&ctl->mmaDone), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
@@ -926,6 +995,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         }
         named_bar_sync(1, kConsumers * 32);   // (B) the four warp states are in shared memory
         write_split_partial(a, part, smem, ctl, threadIdx.x - kFirstConsumer * 32);
+        finish_split(a, b, h, smem, ctl, threadIdx.x - kFirstConsumer * 32);
     }
 }
 
@@ -979,8 +1049,11 @@ int device_sms() {
 void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split) {
     const int sms = device_sms();
     // kCtasPerSm CTAs fit per SM; split 0 of every (sequence, kv head) is the
-    // BF16 sink/tail CTA, so a single wave holds units * (splits + 1) CTAs
-    const int slots = kCtasPerSm * sms;
+    // BF16 sink/tail CTA, so a single wave holds units * (splits + 1) CTAs.
+    // A few slots stay free for the query quantizer of the next call (one CTA
+    // per sequence, launched early): a decode CTA that found no slot would
+    // start late and hold up the whole layer.
+    const int slots = kCtasPerSm * sms - min(max(B, 1), 8);
     const int units = max(1, B * hkv);
     int ns = max(1, slots / units - 1);
     ns = max(1, min(ns, max(1, max_blocks)));
@@ -999,8 +1072,25 @@ void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_s
     *pages_per_split = pps;
 }
 
-size_t decode_ws_bytes(int B, int hq, int nsplit) {
+size_t decode_parts_bytes(int B, int hq, int nsplit) {
     return (size_t)B * hq * (nsplit + 1) * kPartStride * sizeof(float);
+}
+
+size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit) {
+    // the split partials, then one 8-byte arrival counter per (sequence, kv head)
+    return decode_parts_bytes(B, hq, nsplit) + (size_t)B * hkv * sizeof(unsigned long long);
+}
+
+unsigned long long next_decode_tag() {
+    // Call n gets tag n * K mod 2^40 (K odd: a bijection on 40-bit numbers,
+    // so no two of the first 2^40 calls share a tag, and consecutive tags are
+    // far apart); tag 0 would be call 2^40 and is skipped.
+    static std::atomic<unsigned long long> calls{0};
+    for (;;) {
+        const unsigned long long n = calls.fetch_add(1) + 1;
+        const unsigned long long t = (n * 0x9E3779B97Full) & ((1ull << 40) - 1);
+        if (t != 0) return t;
+    }
 }
 
 using DecodeFn = void (*)(DecodeArgs);
@@ -1041,13 +1131,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
-    if (e != cudaSuccess) return e;
-    // the split combine, dependent on the decode grid
-    cfg.gridDim = dim3((unsigned)(a.B * a.hq));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // ------------------------------------------- fixed scratch (no allocation) --

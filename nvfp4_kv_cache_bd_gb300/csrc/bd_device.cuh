@@ -109,6 +109,20 @@ __device__ __forceinline__ float div6(float a) {
     return __fmaf_rn(r, y, q0);
 }
 
+// The E4M3 scale byte of a / 6 for a probability block maximum a in [0, 8]:
+// the same byte as e4m3(RN(a / 6)), without div6's branch (so the blocks of a
+// page can be scheduled together).  For a >= 2^-100 the Markstein steps give
+// RN(a / 6) itself; for smaller a they give a non-negative value below
+// 2^-100, which rounds to the zero byte exactly as RN(a / 6) does (E4M3's
+// smallest nonzero value is 2^-9).  Checked against e4m3(__fdiv_rn(a, 6)) for
+// every binary32 a in [0, 8] by tests/div6_check.cu.
+__device__ __forceinline__ uint32_t e4m3_div6(float a) {
+    const float y = 1.0f / 6.0f;
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, 6.0f, a);
+    return e4m3(__fmaf_rn(r, y, q0));
+}
+
 // ------------------------------------------------------------- f16x2 math --
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {

@@ -67,6 +67,8 @@ struct DecodeArgs {
     const uint16_t* tail_v;
     float* out;
     float* parts;             // [B][Hq][nsplit + 1][kPartStride]
+    unsigned long long* counters;   // [B][Hkv] split arrival counters (tag << 24 | count)
+    unsigned long long tag;   // this call's 40-bit counter tag (never 0)
     int* err;
     size_t qstride;
     int B, hq, hkv, max_blocks, nsplit, pages_per_split;
@@ -80,7 +82,9 @@ cudaError_t launch_query(const QueryArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);
 void decode_splits(int B, int hkv, int max_blocks, int* nsplit, int* pages_per_split);
-size_t decode_ws_bytes(int B, int hq, int nsplit);
+size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit);
+size_t decode_parts_bytes(int B, int hq, int nsplit);
+unsigned long long next_decode_tag();
 
 // Fixed device scratch of bd_decode_attention_noalloc (see bd_decode.cu).
 constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;

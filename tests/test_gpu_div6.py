@@ -1,7 +1,9 @@
-"""The decode's division by 6 (Markstein's correction step after a
-multiplication by RN(1/6)) equals CUDA's correctly rounded __fdiv_rn(a, 6)
-for every binary32 a in [0, 8]: the check program compiles the library's own
-device helper and compares all 1,090,519,041 inputs on the GPU."""
+"""The division by 6 (Markstein's correction step after a multiplication by
+RN(1/6)) equals CUDA's correctly rounded __fdiv_rn(a, 6) for every binary32 a
+in [0, 8], and the decode's branch-free E4M3 scale byte of a / 6 equals the
+byte of that correctly rounded quotient: the check program compiles the
+library's own device helpers and compares all 1,090,519,041 inputs on the
+GPU."""
 import os
 import subprocess
 import tempfile
@@ -23,3 +25,4 @@ def test_div6_matches_ieee_division_on_all_block_maxima():
     words = out.split()
     assert words[0] == "checked" and int(words[1]) == 0x41000001, out
     assert int(words[3]) == 0, out
+    assert words[6:8] == ["scale", "mismatches"] and int(words[8]) == 0, out
