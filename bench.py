@@ -5,7 +5,9 @@ Headline workload (the metric's configuration): single-sequence decode at a
 recipe (16-token BF16 sink, Hadamard + centered keys with {4,6} scales,
 two-term query, FP4 probabilities with c = 8, tau = 1.0), 128-token pages
 with a shuffled physical block table.  One timed step = for each of the 36
-layers, bd_quantize_query + bd_decode_attention, replayed as one CUDA graph.
+layers, one bd_decode_attention call on the raw bf16 query (the decode kernel
+quantizes it: the bytes bd_quantize_query would write), replayed as one CUDA
+graph; --two-call times bd_quantize_query + bd_decode_attention instead.
 
 The same run also times, each on its own workload and with its own clock
 window, every other configuration of the workload table ("configs" in the
@@ -56,6 +58,9 @@ def parse():
     ap.add_argument("--config-steps", type=int, default=0,
                     help="timed steps of each other configuration (default: --steps, at most 100)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--two-call", action="store_true",
+                    help="each layer as bd_quantize_query + bd_decode_attention on the packed query (default: one "
+                         "bd_decode_attention call that quantizes the query itself)")
     return ap.parse_args()
 
 
@@ -152,13 +157,14 @@ class DecodeWorkload:
     sequences from one shared pool.  fmt / recipe select the scale format and
     whether keys are rotated and centered."""
 
-    def __init__(self, lens, layers, tau, device, seed=0, fmt=0, recipe=True):
+    def __init__(self, lens, layers, tau, device, seed=0, fmt=0, recipe=True, two_call=False):
         import torch
         import nvfp4_kv_cache_bd_gb300 as bd
         from nvfp4_kv_cache_bd_gb300 import synth
         if isinstance(lens, int):
             lens = [lens]
         self.bd, self.torch = bd, torch
+        self.two_call = two_call
         self.layers, self.tau = layers, tau
         self.B = B = len(lens)
         self.ctx = bd.Context(bd.make_config(num_layers=layers, format=fmt, rotation=int(recipe),
@@ -219,17 +225,21 @@ class DecodeWorkload:
         self.bytes_per_layer = self.npages * HKV * 2 * self.rec
 
     def layer(self, l, stream=None, q=None, ev=None, out=None):
+        """One layer: bd_decode_attention on the raw query, which quantizes it
+        inside the decode (fused, the default), or bd_quantize_query then
+        bd_decode_attention on the packed query (two_call)."""
         bd = self.bd
         q = self.qs[l] if q is None else q
         out = self.out[l] if out is None else out
-        bd.quantize_query(self.ctx, l, q, self.qp[l], stream)
+        if self.two_call:
+            bd.quantize_query(self.ctx, l, q, self.qp[l], stream)
         if ev is not None:
             ev[0].record()
         sk, sv = self.sinks[l]
         tk, tv = self.tails[l]
         gk, gv = self.gscales[l]
-        bd.decode_attention(self.ctx, l, self.qp[l], q, self.pools[l], self.block_table, self.seq_lens, sk, sv,
-                            tk, tv, self.tau, gk, gv, out, self.ws, stream)
+        bd.decode_attention(self.ctx, l, self.qp[l] if self.two_call else None, q, self.pools[l], self.block_table,
+                            self.seq_lens, sk, sv, tk, tv, self.tau, gk, gv, out, self.ws, stream)
         if ev is not None:
             ev[1].record()
 
@@ -461,15 +471,18 @@ def main():
     cfg_steps = args.config_steps or min(args.steps, 100)
 
     # ---------------- decode workload (headline)
-    wl = DecodeWorkload(args.ctx, args.layers, args.tau, device, seed=rank)
+    wl = DecodeWorkload(args.ctx, args.layers, args.tau, device, seed=rank, two_call=args.two_call)
     step_bytes = wl.bytes_per_layer * args.layers
     assert step_bytes > L2_BYTES, "a step must stream more than L2 holds"
     fn = graphed(lambda: wl.step(), torch)   # one step = 36 x (query quantization + decode)
     ms = timed(fn, args.steps, args.warmup, stream, torch, pg, clocks)
-    # the decode alone inside a graphed step (packed queries left by the step
-    # above): its per-layer time is the decode launch's in-step duration
-    dec_graph_ms = timed(graphed(lambda: wl.decode_step(), torch), args.steps, args.warmup, stream, torch, pg,
-                         clocks)
+    if args.two_call:
+        # the decode alone inside a graphed step (packed queries left by the
+        # step above): its per-layer time is the decode launch's in-step duration
+        dec_graph_ms = timed(graphed(lambda: wl.decode_step(), torch), args.steps, args.warmup, stream, torch, pg,
+                             clocks)
+    else:
+        dec_graph_ms = ms   # the step is the layers' decode calls alone
     # stream-ordered, one decode call at a time with events around it
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.layers)]
     durs = []
@@ -538,11 +551,13 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "packed_kv_gbs": job_rate(step_bytes, ms, world) / 1e9,
         "packed_kv_frac_of_peak": job_rate(step_bytes, ms, world) / 1e9 / (hbm_peak * world),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel + combine_kernel (one bd_decode_attention call)",
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel (one bd_decode_attention call"
+                               + (")" if args.two_call else ", query quantization inside)"),
                      "achieved": achieved_in_step, "peak": hbm_peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved_in_step / hbm_peak,
-                     "frac_basis": (f"in step: one graph of the {args.layers} layers' decode calls alone (packed "
-                                    f"queries in place), {dec_graph_ms * 1000:.1f} us / {args.layers} = "
+                     "frac_basis": (f"in step: one graph of the {args.layers} layers' decode calls alone"
+                                    + (" (packed queries in place)" if args.two_call else "")
+                                    + f", {dec_graph_ms * 1000:.1f} us / {args.layers} = "
                                     f"{in_step_ms * 1000:.2f} us per call"),
                      "frac_in_step": achieved_in_step / hbm_peak, "us_per_call_in_step": in_step_ms * 1000,
                      "frac_call": achieved_call / hbm_peak, "achieved_call": achieved_call,

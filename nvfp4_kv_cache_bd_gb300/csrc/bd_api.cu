@@ -226,8 +226,9 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     if (!finite_in(tau, 0.0f, 448.0f)) return BD_ERR_INVALID_ARG;
     if (!finite_in(k_gscale, 1e-30f, 1e30f) || !finite_in(v_gscale, 1e-30f, 1e30f)) return BD_ERR_INVALID_ARG;
     if (B == 0) return BD_OK;
-    if (!q_packed || !q || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v || !out || !ws)
-        return BD_ERR_INVALID_ARG;
+    if (!q || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v || !out || !ws) return BD_ERR_INVALID_ARG;
+    // no packed query: the decode quantizes q itself, for up to 32 query heads
+    if (!q_packed && ctx->cfg.num_q_heads > 32) return BD_ERR_UNSUPPORTED;
     if (max_blocks > 0 && (!block_table || !kv_pool)) return BD_ERR_INVALID_ARG;
     const uintptr_t align = (uintptr_t)q_packed | (uintptr_t)kv_pool | (uintptr_t)q | (uintptr_t)sink_k |
                             (uintptr_t)sink_v | (uintptr_t)tail_k | (uintptr_t)tail_v | (uintptr_t)out | (uintptr_t)ws;
@@ -238,6 +239,9 @@ int bd_decode_attention(bd_ctx* ctx, int layer, const void* q_packed, const void
     bd::DecodeArgs a;
     a.qp = static_cast<const uint8_t*>(q_packed);
     a.q = static_cast<const uint16_t*>(q);
+    a.mu = layer_mu(ctx, layer);
+    a.rotation = ctx->cfg.rotation;
+    a.terms = ctx->cfg.query_terms;
     a.pool = static_cast<const uint8_t*>(kv_pool);
     a.block_table = block_table;
     a.seq_lens = seq_lens;
@@ -279,7 +283,8 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     if (!finite_in(tau, 0.0f, 448.0f)) return BD_ERR_INVALID_ARG;
     if (!finite_in(k_gscale, 1e-30f, 1e30f) || !finite_in(v_gscale, 1e-30f, 1e30f)) return BD_ERR_INVALID_ARG;
     if (B == 0) return BD_OK;
-    if (!q_packed || !q || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v || !out) return BD_ERR_INVALID_ARG;
+    if (!q || !seq_lens || !sink_k || !sink_v || !tail_k || !tail_v || !out) return BD_ERR_INVALID_ARG;
+    if (!q_packed && ctx->cfg.num_q_heads > 32) return BD_ERR_UNSUPPORTED;
     if (max_blocks > 0 && (!block_table || !kv_pool)) return BD_ERR_INVALID_ARG;
     const uintptr_t align = (uintptr_t)q_packed | (uintptr_t)kv_pool | (uintptr_t)q | (uintptr_t)sink_k |
                             (uintptr_t)sink_v | (uintptr_t)tail_k | (uintptr_t)tail_v | (uintptr_t)out;
@@ -301,6 +306,11 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
     bd::DecodeArgs a;
     a.qp = static_cast<const uint8_t*>(q_packed);
     a.q = static_cast<const uint16_t*>(q);
+    // this path never creates the key-mean array: without it no shift was set
+    // (q.mu = 0)
+    a.mu = ctx->d_mu ? layer_mu(ctx, layer) : nullptr;
+    a.rotation = ctx->cfg.rotation;
+    a.terms = ctx->cfg.query_terms;
     a.pool = static_cast<const uint8_t*>(kv_pool);
     a.block_table = block_table;
     a.seq_lens = seq_lens;

@@ -63,6 +63,7 @@
 #include <mutex>
 
 #include "bd_device.cuh"
+#include "bd_query.cuh"
 
 namespace bd {
 namespace {
@@ -112,6 +113,7 @@ struct alignas(16) Ctl {
     unsigned long long sfbFree[kSfbSlots];                // a K scale-factor slot's MMAs completed
     unsigned long long mmaDone;                   // every MMA the CTA issued has completed
     unsigned long long mergeBar;                  // the merging split's staged partials arrived
+    float qred[kThreads / 32];                    // fused query: per-warp amax
     float wm[kConsumers + 1][4];   // per-warp running max per head (log2 units); last: BF16 tokens
     float wl[kConsumers + 1][4];   // per-warp softmax denominator per head
     int abort_flag;
@@ -123,10 +125,14 @@ constexpr int kCtlBytes = (int)((sizeof(Ctl) + 127) / 128 * 128);
 constexpr int kTabOff = kRingBytes + kCtlBytes;      // probability-quantizer tables (1 KB)
 constexpr int kQiOff = kTabOff + 1024;               // query operand image (28 x 512 B)
 constexpr int kSfaOff = kQiOff + kQiGroups * 512;    // query scale-factor groups (2 x 512 B)
-constexpr int kSmemBytes = kSfaOff + 1024;
+constexpr int kQpOff = kSfaOff + 1024;               // fused query: the token's packed query record
+constexpr int kFusedMaxHq = 32;                      // fused query quantization up to this many query heads
+constexpr int kFusedQpBytes = 4864;                  // the packed record of kFusedMaxHq heads
+static_assert(kFusedQpBytes == (kFusedMaxHq * (2 * 64 + 2 * 8 + 4) + 16 + 255) / 256 * 256, "packed query bytes");
+constexpr int kSmemBytes = kQpOff + kFusedQpBytes;
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 static_assert(kRingBytes % 128 == 0 && kTabOff % 128 == 0 && kQiOff % 128 == 0 && kSfaOff % 128 == 0 &&
-                  kMaxRec % 128 == 0,
+                  kQpOff % 128 == 0 && kMaxRec % 128 == 0,
               "ring slots, tables and operand areas start on 128-byte boundaries");
 // Merge area in the (drained) ring: the O of each consumer warp and of the
 // BF16 tokens, [kConsumers + 1][4 heads][128] floats; the BF16 staging follows.
@@ -314,6 +320,32 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
     }
 }
 
+// ------------------------------------------- FP4 page split: the producers --
+
+// Producer lane: copy page k's K record (isK) or V record into its ring slot
+// k % ring size, whose previous fill has been released.
+template <int FMT>
+__device__ __forceinline__ void fill_slot(const DecodeArgs& a, int h, const int32_t* bt, uint8_t* smem, Ctl* ctl,
+                                          bool isK, int k, uint64_t policy) {
+    constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
+    const int s = k % (isK ? kNK : kNV);
+    const uint32_t full = smem_u32(isK ? &ctl->fullK[s] : &ctl->fullV[s]);
+    uint8_t* slot = smem + (isK ? s : kNK + s) * kMaxRec;
+    const int64_t phys = bt[k];
+    // tag the fill before it is armed: consumers accept a completed phase
+    // only together with their own page index
+    st_release_shared(isK ? &ctl->tagK[s] : &ctl->tagV[s], k);
+    if (page_ok(phys, a.pool_pages)) {
+        const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
+        mbar_arrive_expect_tx(full, RB);
+        bulk_g2s_hint(smem_u32(slot), rec, RB, full, policy);
+    } else {
+        // an entry outside the pool: complete the phase without data
+        if (isK) record_error(a.err, BD_ERR_INVALID_ARG);
+        mbar_arrive(full);
+    }
+}
+
 // ------------------------------------------------ FP4 page split: the MMA --
 
 // Lane 0 of warp 2: the query's scale factors into TMEM, then per round of
@@ -402,8 +434,13 @@ __device__ void mma_rounds(const DecodeArgs& a, int n, const int32_t* bt, uint8_
 template <int FMT>
 __device__ void issue_qk(const DecodeArgs& a, int b, int h, int n, const int32_t* bt, uint8_t* smem, Ctl* ctl,
                          int lane) {
-    griddep_wait();   // the packed query may come from the preceding grid
-    const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
+    const uint8_t* qrec;
+    if (a.qp) {
+        griddep_wait();   // the packed query may come from the preceding grid
+        qrec = a.qp + (size_t)b * a.qstride;
+    } else {
+        qrec = smem + kQpOff;   // quantized by the whole CTA before the roles split
+    }
     const int hq = a.hq;
     uint8_t* Qi = smem + kQiOff;
     uint8_t* Sf = smem + kSfaOff;
@@ -447,11 +484,9 @@ __device__ void issue_qk(const DecodeArgs& a, int b, int h, int n, const int32_t
 // record: lane (g, t) holds dims 16 g .. 16 g + 15 of heads 2 t, 2 t + 1 when
 // t < 2).
 template <int FMT, int PM>
-__device__ void consume_pages(const DecodeArgs& a, int b, int h, int n, const int32_t* bt, uint8_t* smem, Ctl* ctl,
-                              int w, int lane) {
+__device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, int n, const int32_t* bt, uint8_t* smem,
+                              Ctl* ctl, int w, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    griddep_wait();
-    const uint8_t* qrec = a.qp + (size_t)b * a.qstride;
     const int hq = a.hq;
     const float* gq = reinterpret_cast<const float*>(qrec + 2 * hq * 64 + 2 * hq * 8);
     // score = a1 * (Q1 . K) + a2 * (Q2 . K) + q.mu, in log2 units (MXFP4:
@@ -888,7 +923,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 
     const int n = p1 - p0;
     const int32_t* bt = a.block_table + (size_t)b * a.max_blocks + p0;
-    constexpr int RB = (FMT == BD_FORMAT_NVFP4) ? 9216 : 8704;
     if (warp == 3) tmem_alloc(smem_u32(&ctl->tmem), kTmemCols);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNK; ++s) {
@@ -924,6 +958,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (!a.qp) {
+        // Fused query: the rings are empty, so the producers fill them now
+        // (the pages do not depend on the preceding grid); then the whole CTA
+        // quantizes this token's query into shared memory -- the bytes
+        // bd_quantize_query writes -- one (head, 16-dim chunk) item a thread.
+        if (warp < 2 && lane == 0) {
+            const bool isK = (warp == 0);
+            const uint64_t policy = l2_evict_first_policy();
+            for (int k = 0; k < min(n, isK ? kNK : kNV); ++k) fill_slot<FMT>(a, h, bt, smem, ctl, isK, k, policy);
+        }
+        __syncwarp();
+        griddep_wait();   // q may come from the preceding grid
+        QueryArgs qa;
+        qa.q = a.q;
+        qa.mu = a.mu;
+        qa.qp = nullptr;
+        qa.B = a.B;
+        qa.hq = a.hq;
+        qa.format = FMT;
+        qa.rotation = a.rotation;
+        qa.centering = a.centering;
+        qa.terms = a.terms;
+        qa.stride = a.qstride;
+        qquant::quantize_token<1>(qa, a.q + (size_t)b * a.hq * kD, a.mu, smem + kQpOff, (int)threadIdx.x, kThreads,
+                                  ctl->qred, [] { __syncthreads(); });
+        __syncthreads();   // the record is complete
+    }
     // Each warpgroup keeps its own register share to the end: the control
     // warpgroup gives registers back, the consumer warpgroup takes them, and
     // the two branches never merge again (code after a merge would have to
@@ -940,11 +1001,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
             unsigned long long* fullb = isK ? ctl->fullK : ctl->fullV;
             unsigned long long* emptyb = isK ? ctl->emptyK : ctl->emptyV;
             int* tag = isK ? ctl->tagK : ctl->tagV;
-            uint8_t* slots = smem + (isK ? 0 : kNK * kMaxRec);
             if (lane == 0) {
                 // each page is read once per call: evict it from L2 first
                 const uint64_t policy = l2_evict_first_policy();
-                for (int k = 0; k < n; ++k) {
+                // with the fused query the rings were filled before the roles split
+                for (int k = a.qp ? 0 : min(n, N); k < n; ++k) {
                     const int s = k % N;
                     if (k >= N && !mbar_wait_bounded(smem_u32(&emptyb[s]), ((k / N) - 1) & 1, kWaitLimitNs,
                                                      &ctl->abort_flag)) {
@@ -952,20 +1013,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
                         ctl->abort_flag = 1;
                         break;
                     }
-                    const int64_t phys = bt[k];
-                    const uint32_t full = smem_u32(&fullb[s]);
-                    // tag the fill before it is armed: consumers accept a
-                    // completed phase only together with their own page index
-                    st_release_shared(&tag[s], k);
-                    if (page_ok(phys, a.pool_pages)) {
-                        const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
-                        mbar_arrive_expect_tx(full, RB);
-                        bulk_g2s_hint(smem_u32(slots + s * kMaxRec), rec, RB, full, policy);
-                    } else {
-                        // an entry outside the pool: complete the phase without data
-                        if (isK) record_error(a.err, BD_ERR_INVALID_ARG);
-                        mbar_arrive(full);
-                    }
+                    fill_slot<FMT>(a, h, bt, smem, ctl, isK, k, policy);
                 }
             }
             __syncthreads();   // (A)
@@ -988,7 +1036,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
         const int q = warp - kFirstConsumer;
-        consume_pages<FMT, PM>(a, b, h, n, bt, smem, ctl, q, lane);   // contains (A)
+        griddep_wait();   // the packed query may come from the preceding grid
+        const uint8_t* qrec = a.qp ? a.qp + (size_t)b * a.qstride : smem + kQpOff;
+        consume_pages<FMT, PM>(a, qrec, h, n, bt, smem, ctl, q, lane);   // contains (A)
         if (q == 0 && lane < 4) {   // no BF16 tokens in an FP4 split
             ctl->wm[kConsumers][lane] = -INFINITY;
             ctl->wl[kConsumers][lane] = 0.0f;

@@ -56,8 +56,10 @@ struct QueryArgs {
 };
 
 struct DecodeArgs {
-    const uint8_t* qp;
+    const uint8_t* qp;        // packed query; nullptr: the decode quantizes q itself
     const uint16_t* q;
+    const float* mu;          // the layer's key mean [Hkv][128] (fused query quantization)
+    int rotation, terms;      // query recipe (fused query quantization)
     const uint8_t* pool;
     const int32_t* block_table;
     const int32_t* seq_lens;

@@ -113,7 +113,10 @@ def qmu_of(c: Case, qp: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(qp[:, off:off + 4 * HQ]).view(np.float32)
 
 
-def run_gpu(c: Case, dev="cuda", stream=None, pool=None) -> dict:
+def run_gpu(c: Case, dev="cuda", stream=None, pool=None, fused_query=False) -> dict:
+    """The library path: writer, query quantizer, decode.  fused_query: the
+    decode takes no packed query and quantizes q itself (the packed query is
+    still produced, for the fields compared elsewhere)."""
     B = len(c.spec.lens)
     bd.set_key_shift(c.ctx, 0, c.mu)
     g = lambda t: t.to(dev)
@@ -131,7 +134,8 @@ def run_gpu(c: Case, dev="cuda", stream=None, pool=None) -> dict:
     out = torch.full((B, HQ, D), float("nan"), dtype=torch.float32, device=dev)
     ws = torch.zeros(max(1, bd.decode_workspace_size(c.ctx, B, bt.shape[1])) // 4 + 1, dtype=torch.float32,
                      device=dev)
-    bd.decode_attention(c.ctx, 0, qp, q, pool, bt, sl, sk, sv, tk, tv, c.spec.tau, c.gk, c.gv, out, ws, stream)
+    bd.decode_attention(c.ctx, 0, None if fused_query else qp, q, pool, bt, sl, sk, sv, tk, tv, c.spec.tau, c.gk,
+                        c.gv, out, ws, stream)
     torch.cuda.synchronize()
     res = dict(pool=pool.cpu().numpy(), qp=qp.cpu().numpy(), out=out.cpu().double().numpy())
     res["bf16_unchanged"] = all(torch.equal(a.cpu(), b) for a, b in

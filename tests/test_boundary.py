@@ -128,8 +128,20 @@ def test_null_and_range_arguments(L):
     assert L.bd_decode_attention(*args(1.0, gk=math.nan)) == bd.ERR_INVALID_ARG
     assert L.bd_decode_attention(*args(1.0, ws_bytes=ws_need - 1)) == bd.ERR_WORKSPACE
     bad = list(args(1.0))
-    bad[2] = None  # q_packed
+    bad[3] = None  # q (raw query)
     assert L.bd_decode_attention(*bad) == bd.ERR_INVALID_ARG
+    # no packed query: the decode quantizes q itself (checks pass; with no
+    # GPU here the launch then fails), for up to 32 query heads
+    bad = list(args(1.0))
+    bad[2] = None
+    assert L.bd_decode_attention(*bad) != bd.ERR_INVALID_ARG
+    wide = bd.Context(bd.make_config(num_layers=1, num_q_heads=64, num_kv_heads=16))
+    assert wide.cfg.num_q_heads == 64
+    wargs = list(args(1.0, ws_bytes=L.bd_decode_workspace_size(wide.handle, 1, 4)))
+    wargs[0] = wide.handle
+    wargs[2] = None
+    assert L.bd_decode_attention(*wargs) == bd.ERR_UNSUPPORTED
+    wide.close()
     assert L.bd_set_key_shift(h, 5, fake) == bd.ERR_INVALID_ARG
     assert L.bd_selftest_bounded_wait(h, 0, s) == bd.ERR_INVALID_ARG
     assert L.bd_read_device_error(h, s, None) == bd.ERR_INVALID_ARG

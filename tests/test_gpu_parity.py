@@ -328,3 +328,20 @@ def test_negative_and_overlong_lengths():
     assert not o[0].any()
     mx, rl = cases.attn_errors(o, ref)
     assert mx < MAX_ABS and rl < REL_L2, (mx, rl)
+
+
+@pytest.mark.parametrize("fmt,rotation,centering,terms", [(0, 1, 1, 2), (1, 1, 1, 2), (0, 0, 0, 1), (1, 1, 0, 1),
+                                                          (0, 1, 1, 1)])
+def test_fused_query_matches_the_two_calls(fmt, rotation, centering, terms):
+    """bd_decode_attention without a packed query quantizes the query inside
+    the decode with the same code and order as bd_quantize_query, so the
+    output is bit-identical to quantize_query followed by the decode; it also
+    meets the oracle's tolerance."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 7 + 5, 300, 16 + 128 * 12], seed=140 + fmt + 2 * terms, fmt=fmt,
+                               rotation=rotation, centering=centering, terms=terms))
+    two = cases.run_gpu(c)
+    one = cases.run_gpu(c, fused_query=True)
+    assert np.array_equal(one["out"], two["out"]), np.nanmax(np.abs(one["out"] - two["out"]))
+    ora = cases.run_oracle(c)
+    mx, rl = cases.attn_errors(one["out"], ora["out"])
+    assert mx < MAX_ABS and rl < REL_L2
