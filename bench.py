@@ -565,11 +565,13 @@ def main():
                      "traffic": decode_traffic(args), "bytes_per_launch": wl_bytes_note(args)},
         "e2e": {"value": e2e_ms * 1000.0, "unit": "µs/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        # per layer: the query kernel, then bd_decode_attention's decode and
-        # split-combine kernels
-        "gpu_launches": args.steps * args.layers * 3,
-        "launch": (f"one CUDA graph per step ({args.layers} x query, decode and split-combine kernels, "
-                   "programmatic dependent launch)"),
+        # per layer: bd_decode_attention's one decode kernel (splits merged and,
+        # unless --two-call, the query quantized inside it); --two-call adds
+        # the query kernel
+        "gpu_launches": args.steps * args.layers * (2 if args.two_call else 1),
+        "launch": (f"one CUDA graph per step ({args.layers} x "
+                   + ("query kernel + decode kernel" if args.two_call else "decode kernel") +
+                   ", programmatic dependent launch)"),
         "clocks": clk,
         "writer": writer,
     }
@@ -594,8 +596,8 @@ def main():
 # run of this bench; a launch's traffic does not depend on the layer count.
 # Valid only for the kernel sources it was taken on: reported as null once
 # their hash differs.
-DECODE_TRAFFIC = {"sources_sha256_16": "097dabdb6bfb0274", "ctx": 131072, "bytes": 151460608 + 3385856}
-DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h")
+DECODE_TRAFFIC = {"sources_sha256_16": "31548c59682245ef", "ctx": 131072, "bytes": 151565312 + 3495424}
+DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cuh")
 
 
 def decode_sources_hash():
