@@ -667,14 +667,14 @@ def run_configs(args, device, stream, torch, bd, pg, hbm_peak, clocks, steps):
     """The other configurations of the workload table, each a full step."""
     from nvfp4_kv_cache_bd_gb300 import synth
     out = {}
-    wl = DecodeWorkload(4096, 1, 1.0, device)
+    wl = DecodeWorkload(4096, 1, 1.0, device, two_call=args.two_call)
     r = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak, clocks)
     r["note"] = ("4096-token context, 1 layer (the parity configuration): 4.6 MB of packed K/V, inside L2, so this "
                  "is a latency figure, not a bandwidth one")
     out["decode_4k_ctx_1_layer"] = r
     del wl
     out["writer_mxfp4"] = bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=1, clocks=clocks)
-    wl = DecodeWorkload(32768, args.layers, 1.0, device)
+    wl = DecodeWorkload(32768, args.layers, 1.0, device, two_call=args.two_call)
     assert wl.bytes_per_layer * wl.layers > L2_BYTES
     out[f"decode_32k_ctx_{args.layers}_layers"] = step_rate(wl, steps, args.warmup, stream, torch, pg, hbm_peak,
                                                             clocks)
@@ -684,7 +684,7 @@ def run_configs(args, device, stream, torch, bd, pg, hbm_peak, clocks, steps):
     batch = {"lengths": "32 seqs, log-uniform in [1024, 65536], %d tokens in all" % sum(lens)}
     for fmt, fname in ((0, "nvfp4"), (1, "mxfp4")):
         for recipe in (True, False):
-            wl = DecodeWorkload(lens, args.layers, 1.0, device, fmt=fmt, recipe=recipe)
+            wl = DecodeWorkload(lens, args.layers, 1.0, device, fmt=fmt, recipe=recipe, two_call=args.two_call)
             batch[f"{fname}_{'rotation_centering' if recipe else 'plain_keys'}"] = step_rate(
                 wl, steps, args.warmup, stream, torch, pg, hbm_peak, clocks)
             del wl

@@ -215,13 +215,19 @@ int bd_append_kv(bd_ctx* ctx, int layer, const void* k_new, const void* v_new, c
                  void* tail_v, int B, float k_gscale, float v_gscale, void* kv_pool, void* stream);
 
 /* Workspace bytes bd_decode_attention needs for B sequences whose block
- * table rows hold max_blocks entries (0 if B == 0): the split partials and
- * one 8-byte arrival counter per (sequence, kv head). */
+ * table rows hold max_blocks entries (0 if B == 0): the split partials, one
+ * 8-byte arrival counter per (sequence, kv head) and room for B packed
+ * queries. */
 size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
 
 /* Paged single-token decode attention over the hybrid cache ([arch] decode
  * interface -> paged attention kernel; [cfg] sink_tokens, block_size):
- *   q_packed    : from bd_quantize_query, device.
+ *   q_packed    : from bd_quantize_query, device; or NULL (num_q_heads <= 32,
+ *                 else BD_ERR_UNSUPPORTED): the call quantizes q itself into
+ *                 the bytes bd_quantize_query would write -- inside the
+ *                 decode kernel when its grid fits one wave of the GPU, else
+ *                 with the query kernel into ws first -- and the output is
+ *                 bit-identical to passing those bytes.
  *   q           : bf16 [B][num_q_heads][128], device (raw query, used by the
  *                 BF16 sink and tail tokens).
  *   kv_pool     : the layer's pool (layout above), device.
@@ -243,15 +249,18 @@ size_t bd_decode_workspace_size(const bd_ctx* ctx, int B, int max_blocks);
  *   k/v_gscale  : the per-tensor scales the layer's pages were written with.
  *   out         : fp32 [B][num_q_heads][128], device.
  *   ws          : device scratch of at least bd_decode_workspace_size(ctx, B,
- *                 max_blocks) bytes for the split partials and the split
- *                 arrival counters; it needs no initialization (a counter
+ *                 max_blocks) bytes for the split partials, the split
+ *                 arrival counters and (q_packed NULL) the packed queries;
+ *                 it needs no initialization (a counter
  *                 carries a per-call tag: bytes from earlier calls or never
  *                 written count as zero).  Calls that share a workspace must
  *                 not overlap on the GPU.
  * Query head j reads kv head j / 4; softmax scale 1/sqrt(128).
- * One kernel is launched on `stream`: each split writes its partial to ws
- * and counts itself in at its (sequence, kv head)'s counter, and the split
- * that completes the count merges that group's partials into out.
+ * One decode kernel is launched on `stream` (preceded by the query kernel
+ * in the one case above): each split holding pages (and the
+ * split of the BF16 sink and tail) writes its partial to ws and counts
+ * itself in at its (sequence, kv head)'s counter, and the split that
+ * completes the count merges that group's partials into out.
  * Ordering: the kernel may start reading kv_pool, block_table and seq_lens
  * while the preceding grid in the stream, if it allows programmatic early
  * launch, still runs (this library's query and decode kernels do); those

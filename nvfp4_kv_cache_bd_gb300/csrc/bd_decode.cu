@@ -44,9 +44,11 @@
 //            query head; their results are never read.
 // Every page's K and V record is read once from HBM; each page is processed
 // by one warp in a fixed order, so a split's result does not depend on
-// scheduling.  Each split writes its partial (m, l, O per query head) to the
-// workspace and counts itself in at its (sequence, kv head)'s arrival
-// counter; the split that completes the count merges that group's partials,
+// scheduling.  Split 0 and every split with pages write their partial (m,
+// l, O per query head) to the workspace and count themselves in at their
+// (sequence, kv head)'s arrival counter (a split past its sequence's pages
+// exits at once; each CTA knows from the length how many splits hold
+// pages); the split that completes the count merges that group's partials,
 // O = sum 2^(m-M) O / sum 2^(m-M) l, in a fixed split order, so the result
 // does not depend on which split came last either.  With no separate merge
 // kernel, a layer is one grid: nothing of a layer's chain holds an SM slot
@@ -118,6 +120,7 @@ struct alignas(16) Ctl {
     float wl[kConsumers + 1][4];   // per-warp softmax denominator per head
     int abort_flag;
     int last_split;                // this split completed its group's arrival count
+    int nlive;                     // split 0 and the splits with pages of this (sequence, kv head)
     int tagK[kNK], tagV[kNV];      // page index each slot's latest fill holds (-1: none)
     uint32_t tmem;                 // TMEM base address
 };
@@ -756,32 +759,33 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
 // by one compare-and-swap -- it fails only if another split of this call got
 // there first, and every later update keeps this call's tag -- and then each
 // split adds 1 with one atomic add, which the L2 serves without retries.
-__device__ bool count_split_in(const DecodeArgs& a, int b, int h) {
+__device__ bool count_split_in(const DecodeArgs& a, int b, int h, int nlive) {
     unsigned long long* cnt = a.counters + (size_t)b * a.hkv + h;
     const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(cnt);
     if ((w >> 24) != a.tag) atomicCAS(cnt, w, a.tag << 24);
     const unsigned long long old = atomicAdd(cnt, 1ull);
-    return (old & 0xFFFFFFull) == (unsigned long long)a.nsplit;   // nsplit + 1 arrivals in all
+    return (old & 0xFFFFFFull) == (unsigned long long)(nlive - 1);   // nlive arrivals in all
 }
 
-// Merge the nsplit + 1 partials of query heads 4h .. 4h+3 of sequence b into
-// out, by 128 threads tid = 0..127 synchronised on named barrier 1.  G heads
-// at a time (4 when their records fit the ring area, else 2) are staged into
-// shared memory by one bulk asynchronous copy (the TMA unit reads L2, where
-// the other SMs' partials are); warp hh finds head hh's maximum M over the
+// Merge the nlive partials (split 0 and the splits with pages) of query heads
+// 4h .. 4h+3 of sequence b into out, by 128 threads tid = 0..127 synchronised
+// on named barrier 1.  G heads at a time (4 when their records fit the ring
+// area, else 2) are staged into shared memory by bulk asynchronous copies,
+// one per head (the TMA unit reads L2, where the other SMs' partials are);
+// warp hh finds head hh's maximum M over the
 // splits with l > 0 (one integer warp reduction of order-preserving keys), the
 // weights w_s = 2^(m_s - M) and the denominator sum w_s l_s; each thread then
 // sums w_s O_s over its G output dims in split order.  A split with w_s = 0
 // wrote no O (its bytes may hold anything, NaN included): it is skipped.
-__device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ctl* ctl, int tid) {
-    const int nparts = a.nsplit + 1;
+__device__ void merge_group(const DecodeArgs& a, int b, int h, int nlive, uint8_t* smem, Ctl* ctl, int tid) {
+    const int nparts = a.nsplit + 1;   // the workspace's record stride per head
     const int lane = tid & 31, warp = tid >> 5;
-    const int G = (4 * nparts * kPartStride * 4 <= kRingBytes - 4 * 4 * (kMaxSplits + 1)) ? 4 : 2;
-    float* stage = reinterpret_cast<float*>(smem);
-    float* sw = stage + G * nparts * kPartStride;   // [G][kMaxSplits] weights, then [G] denominators
+    const int G = (4 * nlive * kPartStride * 4 <= kRingBytes - 4 * 4 * (kMaxSplits + 1)) ? 4 : 2;
+    float* stage = reinterpret_cast<float*>(smem);   // [G][nlive][kPartStride]
+    float* sw = stage + G * nlive * kPartStride;   // [G][kMaxSplits] weights, then [G] denominators
     float* sden = sw + G * kMaxSplits;
     const uint32_t bar = smem_u32(&ctl->mergeBar);
-    const uint32_t bytes = (uint32_t)(G * nparts * kPartStride * 4);   // a multiple of 16
+    const uint32_t hbytes = (uint32_t)(nlive * kPartStride * 4);   // one head's live records, a multiple of 16
     if (tid == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -791,22 +795,24 @@ __device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ct
     named_bar_sync(1, 128);
     for (int h0 = 0, pass = 0; h0 < 4; h0 += G, ++pass) {
         if (tid == 0) {
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(smem_u32(stage), a.parts + (size_t)(b * a.hq + 4 * h + h0) * nparts * kPartStride, bytes, bar);
+            mbar_arrive_expect_tx(bar, (uint32_t)G * hbytes);
+            for (int hh = 0; hh < G; ++hh)
+                bulk_g2s(smem_u32(stage + hh * nlive * kPartStride),
+                         a.parts + (size_t)(b * a.hq + 4 * h + h0 + hh) * nparts * kPartStride, hbytes, bar);
         }
         if (!mbar_wait_bounded(bar, pass & 1, kWaitLimitNs, nullptr)) {
             if (tid == 0) record_error(a.err, BD_ERR_TIMEOUT);
             return;   // every thread gives up at the same wait
         }
         if (warp < G) {
-            const float* hp = stage + warp * nparts * kPartStride;
+            const float* hp = stage + warp * nlive * kPartStride;
             float m[2], l[2];
             uint32_t key = 0;   // order-preserving key of the largest m with l > 0
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int sidx = lane + 32 * r;
-                m[r] = (sidx < nparts) ? hp[sidx * kPartStride] : -INFINITY;
-                l[r] = (sidx < nparts) ? hp[sidx * kPartStride + 1] : 0.0f;
+                m[r] = (sidx < nlive) ? hp[sidx * kPartStride] : -INFINITY;
+                l[r] = (sidx < nlive) ? hp[sidx * kPartStride + 1] : 0.0f;
                 if (l[r] > 0.0f) key = max(key, f32_order_key(m[r]));
             }
             key = __reduce_max_sync(kFull, key);
@@ -816,7 +822,7 @@ __device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ct
             for (int r = 0; r < 2; ++r) {
                 const int sidx = lane + 32 * r;
                 const float w = (l[r] > 0.0f) ? ex2(m[r] - M) : 0.0f;
-                if (sidx < nparts) sw[warp * kMaxSplits + sidx] = w;
+                if (sidx < nlive) sw[warp * kMaxSplits + sidx] = w;
                 den = fmaf(w, l[r], den);
             }
 #pragma unroll
@@ -826,10 +832,10 @@ __device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ct
         named_bar_sync(1, 128);
         // thread tid: head h0 + tid / (128 / G), G consecutive dims
         const int hh = tid / (128 / G), d0 = (tid % (128 / G)) * G;
-        const float* hp = stage + hh * nparts * kPartStride + 4 + d0;
+        const float* hp = stage + hh * nlive * kPartStride + 4 + d0;
         const float* w = sw + hh * kMaxSplits;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int sidx = 0; sidx < nparts; ++sidx) {
+        for (int sidx = 0; sidx < nlive; ++sidx) {
             const float ws = w[sidx];
             if (ws == 0.0f) continue;
             if (G == 4) {
@@ -863,12 +869,14 @@ __device__ void merge_group(const DecodeArgs& a, int b, int h, uint8_t* smem, Ct
 // was the last of its group, merge the group.
 __device__ void finish_split(const DecodeArgs& a, int b, int h, uint8_t* smem, Ctl* ctl, int tid) {
     __threadfence();   // this thread's partial writes are visible device-wide before the count
+    // split 0 and the splits with pages (set by thread 0 at the kernel's start)
+    const int nlive = ctl->nlive;
     named_bar_sync(1, 128);
-    if (tid == 0) ctl->last_split = count_split_in(a, b, h) ? 1 : 0;
+    if (tid == 0) ctl->last_split = count_split_in(a, b, h, nlive) ? 1 : 0;
     named_bar_sync(1, 128);
     if (!*reinterpret_cast<volatile int*>(&ctl->last_split)) return;
     __threadfence();   // the other splits' partials, counted in before this one
-    merge_group(a, b, h, smem, ctl, tid);
+    merge_group(a, b, h, nlive, smem, ctl, tid);
 }
 
 template <int FMT, int PM>
@@ -897,15 +905,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     const int p0 = bf16 ? 0 : (split - 1) * a.pages_per_split;
     const int p1 = bf16 ? 0 : min(p0 + a.pages_per_split, npages);
 
-    if (p0 >= p1 && !bf16) {
-        griddep_wait();
-        if (threadIdx.x < 4) {
-            part[threadIdx.x * (a.nsplit + 1) * kPartStride + 0] = -INFINITY;
-            part[threadIdx.x * (a.nsplit + 1) * kPartStride + 1] = 0.0f;
-        }
-        if (threadIdx.x < 128) finish_split(a, b, h, smem, ctl, threadIdx.x);
-        return;
-    }
+    // a split past its sequence's pages does nothing: it is neither written
+    // nor counted, and the merge reads split 0 and the nlive - 1 splits with
+    // pages (always the first ones)
+    if (p0 >= p1 && !bf16) return;
+    if (threadIdx.x == 0) ctl->nlive = 1 + (npages + a.pages_per_split - 1) / a.pages_per_split;
     if (bf16) {
         // no FP4 pages: the consumer states are empty and nothing aborted
         if (threadIdx.x < kConsumers * 4) {
@@ -1128,9 +1132,24 @@ size_t decode_parts_bytes(int B, int hq, int nsplit) {
     return (size_t)B * hq * (nsplit + 1) * kPartStride * sizeof(float);
 }
 
+// The workspace: the split partials, one 8-byte arrival counter per
+// (sequence, kv head), then (at a 256-byte boundary) room for the packed
+// queries a call without a packed query may need (below).
+size_t decode_qp_offset(int B, int hq, int hkv, int nsplit) {
+    const size_t end = decode_parts_bytes(B, hq, nsplit) + (size_t)B * hkv * sizeof(unsigned long long);
+    return (end + 255) / 256 * 256;
+}
+
 size_t decode_ws_bytes(int B, int hq, int hkv, int nsplit) {
-    // the split partials, then one 8-byte arrival counter per (sequence, kv head)
-    return decode_parts_bytes(B, hq, nsplit) + (size_t)B * hkv * sizeof(unsigned long long);
+    return decode_qp_offset(B, hq, hkv, nsplit) + (size_t)B * qpack_stride(hq);
+}
+
+// A decode grid that fits one wave (the free slots kept): without a packed
+// query, its CTAs quantize the query themselves; a larger grid would repeat
+// that in every wave, so the query kernel quantizes it into the workspace
+// first.
+bool decode_one_wave(int B, int hkv, int nsplit) {
+    return (long long)max(1, B * hkv) * (nsplit + 1) <= (long long)kCtasPerSm * device_sms() - min(max(B, 1), 8);
 }
 
 unsigned long long next_decode_tag() {
@@ -1173,6 +1192,23 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
             g_dev[dev].smem_attr[f][pm] = true;
         }
     }
+    DecodeArgs da = a;
+    if (!a.qp && !decode_one_wave(a.B, a.hkv, a.nsplit)) {
+        QueryArgs qa;
+        qa.q = a.q;
+        qa.mu = a.mu;
+        qa.qp = reinterpret_cast<uint8_t*>(a.parts) + decode_qp_offset(a.B, a.hq, a.hkv, a.nsplit);
+        qa.B = a.B;
+        qa.hq = a.hq;
+        qa.format = a.format;
+        qa.rotation = a.rotation;
+        qa.centering = a.centering;
+        qa.terms = a.terms;
+        qa.stride = a.qstride;
+        cudaError_t e = launch_query(qa, s);
+        if (e != cudaSuccess) return e;
+        da.qp = qa.qp;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.nsplit + 1), (unsigned)a.hkv, (unsigned)a.B);
     cfg.blockDim = dim3(kThreads);
@@ -1183,7 +1219,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, da);
 }
 
 // ------------------------------------------- fixed scratch (no allocation) --
