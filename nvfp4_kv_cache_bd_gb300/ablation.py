@@ -47,12 +47,16 @@ SCHEMES = [
 ]
 
 # ------------------------------------------------------- host dequantizer --
-# Byte layouts of include/bd.h: a K record is codes[128 tok][64 B] (element
-# d of a token in byte d/2, even d in the low nibble) then scale bytes
-# [128 tok][nb]; a V record is codes[8][8][128 B] where the byte of head dim
-# d in row (i, p) holds token 16i+p (low nibble) and token 16i+p+8 (high
-# nibble) and sits at 16-byte slot (d // 16) ^ 2 (p % 4), then
+# Byte layouts of include/bd.h: a K record is codes in groups of 8 tokens x
+# 32 dims (the byte of dims d, d+1 of token t at (t/8)*512 + (d/32)*128 +
+# (t%8)*16 + (d%32)/2, even d in the low nibble) then nb/4 scale-factor
+# groups of 512 B (block b of token t at 8192 + (b/4)*512 + (t%32)*16 +
+# (t/32)*4 + b%4); a V record is codes[8][8][128 B] where the byte of head
+# dim d in row (i, p) holds token 16i+2p (low nibble) and token 16i+2p+1
+# (high nibble) and sits at 16-byte slot (d // 16) ^ 2 (p % 4), then
 # scales[8][8][nb][2].  nb = 8 E4M3 bytes (NVFP4) or 4 UE8M0 bytes (MXFP4).
+# A packed query (stride S) holds codes[2 terms][Hq][64 B] (K's nibble
+# order), scales[2][Hq][nb], then g1, g2 and q.mu[Hq] as float32.
 
 _E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, 0, -.5, -1, -1.5, -2, -3, -4, -6], np.float64)
 
@@ -96,6 +100,23 @@ def dequantize_pool(pool: np.ndarray, fmt: int, pages: np.ndarray, gk: float, gv
     if fmt == bd.FORMAT_NVFP4:
         k, v = k * gk, v * gv
     return k.transpose(0, 2, 1, 3), v.transpose(0, 2, 1, 3)
+
+
+def dequantize_query(qp: np.ndarray, fmt: int, hq: int = HQ):
+    """-> (Qhat [B][hq][128] fp64, the sum of both terms with their scales in
+    the rotated domain, q.mu [B][hq]) from packed query records [B][S]."""
+    nb = 8 if fmt == bd.FORMAT_NVFP4 else 4
+    B = qp.shape[0]
+    codes = qp[:, :2 * hq * 64].reshape(B, 2, hq, 64)
+    c = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(B, 2, hq, 128)
+    sb = qp[:, 2 * hq * 64:2 * hq * 64 + 2 * hq * nb].reshape(B, 2, hq, nb)
+    goff = 2 * hq * 64 + 2 * hq * 8
+    g = np.ascontiguousarray(qp[:, goff:goff + 8]).view(np.float32).astype(np.float64)      # [B][2]
+    qmu = np.ascontiguousarray(qp[:, goff + 16:goff + 16 + 4 * hq]).view(np.float32).astype(np.float64)
+    terms = _E2M1[c] * np.repeat(_scale(fmt, sb), 128 // nb, axis=-1)
+    if fmt == bd.FORMAT_NVFP4:
+        terms = terms * g[:, :, None, None]
+    return terms.sum(axis=1), qmu
 
 
 def _fwht_rows(x: np.ndarray) -> np.ndarray:
@@ -166,7 +187,7 @@ def run_scheme(data: Data, cfgkw: dict, taus=(1.0,), dev="cuda"):
     torch.cuda.synchronize()
     if bd.read_device_error(ctx) != bd.OK:
         raise RuntimeError("device error word set")
-    return ctx, pool.cpu().numpy(), gk, gv, outs
+    return ctx, pool.cpu().numpy(), qp.cpu().numpy(), gk, gv, outs
 
 
 def key_value_errors(data: Data, cfgkw: dict, pool: np.ndarray, gk: float, gv: float):
@@ -184,6 +205,54 @@ def key_value_errors(data: Data, cfgkw: dict, pool: np.ndarray, gk: float, gv: f
     vref = np.stack([v[16:16 + 128 * n].double().cpu().numpy() for _, v in data.kv])
     rel = lambda a, r: float(np.linalg.norm(a - r) / np.linalg.norm(r))
     return rel(kh, kref), rel(vh, vref)
+
+
+def error_budget(data: Data, cfgkw: dict, pool: np.ndarray, qp: np.ndarray, gk: float, gv: float,
+                 out: np.ndarray, ref: np.ndarray) -> dict:
+    """Where the attention error comes from, on the FP4 pages (the BF16 sink
+    and tail are exact throughout), in fp64 on the host from the library's
+    own bytes:
+
+    - logits: the scores Qhat . Khat (+ q.mu with centering) against the
+      exact q . k, and A1 = softmax attention with those scores, exact P and
+      exact V, against the exact attention A0;
+    - values: A2 = A1 with the dequantized V, against A1;
+    - probabilities: the decode's output (FP4 P, f16 MMAs) against A2.
+    Relative L2 norms; logit_rms in natural-log units (scores / sqrt(d))."""
+    B = len(data.lens)
+    n = data.split[1]
+    fmt = cfgkw["format"]
+    kh, vh = dequantize_pool(pool, fmt, np.arange(B * n), gk, gv)   # stored domain
+    kh = kh.reshape(B, n * 128, H, D)
+    vh = vh.reshape(B, n * 128, H, D)
+    qh, qmu = dequantize_query(qp, fmt)
+    fp = slice(16, 16 + 128 * n)
+    a1 = np.empty_like(ref)
+    a2 = np.empty_like(ref)
+    ds2 = s2 = 0.0
+    cnt = 0
+    for b, (k, v) in enumerate(data.kv):
+        k64, v64 = k.double().cpu().numpy(), v.double().cpu().numpy()
+        q64 = data.q[b].double().cpu().numpy()
+        for j in range(HQ):
+            h = j // (HQ // H)
+            s_ex = k64[:, h] @ q64[j] / math.sqrt(D)
+            s_hat = s_ex.copy()
+            s_hat[fp] = (kh[b, :, h] @ qh[b, j] + (qmu[b, j] if cfgkw["centering"] else 0.0)) / math.sqrt(D)
+            d = s_hat[fp] - s_ex[fp]
+            ds2 += float(d @ d)
+            s2 += float(s_ex[fp] @ s_ex[fp])
+            cnt += d.size
+            p = np.exp(s_hat - s_hat.max())
+            p /= p.sum()
+            a1[b, j] = p @ v64[:, h]
+            vq = v64[:, h].copy()
+            vq[fp] = vh[b, :, h]
+            a2[b, j] = p @ vq
+    rel = lambda x, y: float(np.linalg.norm(x - y) / np.linalg.norm(y))
+    return dict(logit_rms=math.sqrt(ds2 / max(cnt, 1)), logit_rel=math.sqrt(ds2 / max(s2, 1e-300)),
+                logits_rel_l2=rel(a1, ref), values_rel_l2=rel(a2, a1), probabilities_rel_l2=rel(out, a2),
+                total_rel_l2=rel(out, ref))
 
 
 def attention_errors(data: Data, out: np.ndarray, ref: np.ndarray):
@@ -207,21 +276,30 @@ def main():
            "schemes": {}, "tau_sweep": {}}
     print(f"| scheme | K rel-RMSE | V rel-RMSE | attention rel-L2 | attention max-abs |")
     print(f"|---|---|---|---|---|")
+    budgets = {}
     for name, over in SCHEMES:
         kw = dict(BASE, **over)
-        ctx, pool, gk, gv, outs = run_scheme(data, kw, dev=dev)
+        ctx, pool, qp, gk, gv, outs = run_scheme(data, kw, dev=dev)
         ek, ev = key_value_errors(data, kw, pool, gk, gv)
         rl, mx = attention_errors(data, outs[1.0], ref)
-        res["schemes"][name] = dict(config=kw, k_rel_rmse=ek, v_rel_rmse=ev, attn_rel_l2=rl, attn_max_abs=mx)
+        budgets[name] = error_budget(data, kw, pool, qp, gk, gv, outs[1.0], ref)
+        res["schemes"][name] = dict(config=kw, k_rel_rmse=ek, v_rel_rmse=ev, attn_rel_l2=rl, attn_max_abs=mx,
+                                    error_budget=budgets[name])
         print(f"| {name} | {ek:.4f} | {ev:.4f} | {rl:.5f} | {mx:.5f} |")
         ctx.close()
+    print()
+    print("| scheme | logit RMS | logit rel | attention from logits | + values | + probabilities | total |")
+    print("|---|---|---|---|---|---|---|")
+    for name, e in budgets.items():
+        print(f"| {name} | {e['logit_rms']:.4f} | {e['logit_rel']:.4f} | {e['logits_rel_l2']:.4f} | "
+              f"{e['values_rel_l2']:.4f} | {e['probabilities_rel_l2']:.4f} | {e['total_rel_l2']:.4f} |")
     print()
     print("| c | " + " | ".join(f"tau {t:g}" for t in (0, 0.25, 0.5, 1, 2, 4, 8, 448)) + " |")
     print("|---|" + "---|" * 8)
     taus = (0.0, 0.25, 0.5, 1.0, 2.0, 4.0, 8.0, 448.0)
     for c in (1, 8):
         kw = dict(BASE, p_c=c)
-        ctx, _, _, _, outs = run_scheme(data, kw, taus=taus, dev=dev)
+        ctx, _, _, _, _, outs = run_scheme(data, kw, taus=taus, dev=dev)
         row = {}
         for t in taus:
             rl, mx = attention_errors(data, outs[t], ref)

@@ -32,3 +32,18 @@ def test_dequantize_pool_matches_layout_reader(fmt):
 def test_fwht_rows_is_its_own_inverse():
     x = np.random.default_rng(0).standard_normal((3, 5, 128))
     assert np.allclose(ablation._fwht_rows(ablation._fwht_rows(x)), x, atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_dequantize_query_matches_layout_reader(fmt):
+    """The ablation report's query dequantizer (both terms, their scales and
+    g, in the rotated domain) and its q.mu field agree with the test-side
+    reader on queries the oracle packed."""
+    oracle.build()
+    c = cases.build(cases.Spec(lens=[300, 500], seed=6, fmt=fmt))
+    qp = cases.run_oracle(c, pool_only=True)["qp"]
+    qh, qmu = ablation.dequantize_query(qp, fmt)
+    for b in range(qp.shape[0]):
+        ref_q, _, ref_mu, _, _ = layout.query_record(fmt, 32, qp[b])
+        assert np.array_equal(qh[b], ref_q)
+        assert np.array_equal(qmu[b], ref_mu)
