@@ -7,7 +7,8 @@
 // "amax6"), KV_MODES["bitdecoding-mxfp4"] scale_mode "mxfp4_search";
 // freeze-at-fill pages from kv-landlords quant_ab.py (module docstring).
 //
-// Grid: one CTA of 4 warps per (page, kv head, K or V, half page).  The CTA
+// Grid: one CTA of 4 warps per (page, kv head, half page, K or V), the key
+// CTAs first in launch order.  The CTA
 // first stages its 64 bf16 rows in shared memory with coalesced 16-byte
 // asynchronous copies; each warp then owns one 16-token x 128-dim tile and
 // reads its lanes' values from there.
@@ -335,14 +336,18 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, int row0,
 template <int FMT>
 __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) writer_kernel(const WriterArgs a) {
     extern __shared__ __align__(16) uint8_t tile[];   // [kCtaRows tokens][kTilePitch]: this head's bf16 rows
+    // grid (pages x heads, half page, K or V): every K CTA comes before every
+    // V CTA in launch order, so the heavy key tiles all start in the first
+    // wave and the light value tiles fill the slots they leave
     const int pg = blockIdx.x / a.hkv, h = blockIdx.x % a.hkv;
-    const int kv = blockIdx.y;
-    const int row0 = kCtaRows * blockIdx.z;            // first token of this CTA's half page
+    const int kv = blockIdx.z;
+    const int half = blockIdx.y;
+    const int row0 = kCtaRows * half;                  // first token of this CTA's half page
     const int grp = (row0 >> 4) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const size_t tok_stride = (size_t)a.hkv * kD;
     int64_t page;
     const uint16_t* newrow = nullptr;   // append mode: the new token's row, staged as the page's last row
-    const bool reporter = threadIdx.x == 0 && kv == 0 && blockIdx.z == 0;   // one report per page
+    const bool reporter = threadIdx.x == 0 && kv == 0 && half == 0;   // one report per page
     if (a.seq_lens) {
         // append the token at position L (pg is the sequence) ...
         const int L = a.seq_lens[pg];
@@ -353,12 +358,12 @@ __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) w
         const uint16_t* nrow = (kv == 0 ? a.k_new : a.v_new) + ((size_t)pg * a.hkv + h) * kD;
         if (L < kSink) {
             uint16_t* dst = (kv == 0 ? a.sink_k : a.sink_v) + (((size_t)pg * kSink + L) * a.hkv + h) * kD;
-            if (blockIdx.z == 0 && threadIdx.x < 16)
+            if (half == 0 && threadIdx.x < 16)
                 reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(nrow)[threadIdx.x];
             return;
         }
         const int r = (L - kSink) % kPage, p = (L - kSink) / kPage;
-        if (r / kCtaRows == (int)blockIdx.z && threadIdx.x < 16) {
+        if (r / kCtaRows == half && threadIdx.x < 16) {
             uint16_t* dst = (kv == 0 ? a.tail_k : a.tail_v) + (((size_t)pg * kPage + r) * a.hkv + h) * kD;
             reinterpret_cast<uint4*>(dst)[threadIdx.x] = reinterpret_cast<const uint4*>(nrow)[threadIdx.x];
         }
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kCtaThreads, FMT == BD_FORMAT_NVFP4 ? 8 : 4) w
 
 cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s) {
     if (a.n == 0) return cudaSuccess;
-    dim3 grid((unsigned)(a.n * a.hkv), 2, kPage / kCtaRows);
+    dim3 grid((unsigned)(a.n * a.hkv), kPage / kCtaRows, 2);
     if (a.format == BD_FORMAT_NVFP4)
         writer_kernel<BD_FORMAT_NVFP4><<<grid, kCtaThreads, kTileBytes + kSTabBytes, s>>>(a);
     else
