@@ -200,6 +200,7 @@ constexpr int kMaxBf16Tok = kSink + kPage - 1;   // 143
 // tokens of sequence b, left as state slot kConsumers of the CTA merge: O in
 // the merge area, the maximum and denominator in ctl (maximum -inf: no
 // tokens).  Runs on the whole CTA once the ring is no longer in use.
+__device__ void tag_counter(const DecodeArgs& a, int b, int h);   // below, with the split merge
 __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* smem, Ctl* ctl) {
     const int ns = min(L, kSink);
     const int rest = max(0, L - kSink);
@@ -209,6 +210,7 @@ __device__ void bf16_segment(const DecodeArgs& a, int b, int h, int L, uint8_t* 
     const int tid = threadIdx.x;
     // the sink/tail rows and q may be produced by the preceding grid
     griddep_wait();
+    if (tid == 0) tag_counter(a, b, h);   // thread 0 counts this split in
     if (T <= 0) {
         if (tid < 4) {
             ctl->wm[kConsumers][tid] = -INFINITY;
@@ -752,17 +754,26 @@ __device__ void write_split_partial(const DecodeArgs& a, float* part, const uint
     }
 }
 
-// Count this split in at its (sequence, kv head) group's arrival counter and
-// report whether it completed the count.  The counter word holds the call's
-// 40-bit tag over a 24-bit count.  A word with another tag (an earlier
-// call's, or workspace bytes never written) is first re-tagged with count 0
-// by one compare-and-swap -- it fails only if another split of this call got
-// there first, and every later update keeps this call's tag -- and then each
-// split adds 1 with one atomic add, which the L2 serves without retries.
-__device__ bool count_split_in(const DecodeArgs& a, int b, int h, int nlive) {
+// The arrival counter of a (sequence, kv head) group: a word holding the
+// call's 40-bit tag over a 24-bit count.  tag_counter runs once per split, by
+// the thread that later counts the split in, at the split's start (after the
+// dependent-launch wait, so the preceding call's merge is over): a word with
+// another tag (an earlier call's, or workspace bytes never written) is
+// re-tagged with count 0 by one compare-and-swap.  The swap fails only if a
+// split of this call changed the word first, and every such change leaves
+// this call's tag in it (tags do not repeat), so whichever split comes
+// first, the word holds the tag before any split of the call counts in.
+// The read and the swap are thus off the path from a split's last page to
+// the merge, where count_split_in is one atomic add, served by the L2
+// without retries.
+__device__ void tag_counter(const DecodeArgs& a, int b, int h) {
     unsigned long long* cnt = a.counters + (size_t)b * a.hkv + h;
     const unsigned long long w = *reinterpret_cast<volatile unsigned long long*>(cnt);
     if ((w >> 24) != a.tag) atomicCAS(cnt, w, a.tag << 24);
+}
+// Count this split in; true if it completed the count (nlive arrivals).
+__device__ bool count_split_in(const DecodeArgs& a, int b, int h, int nlive) {
+    unsigned long long* cnt = a.counters + (size_t)b * a.hkv + h;
     const unsigned long long old = atomicAdd(cnt, 1ull);
     return (old & 0xFFFFFFull) == (unsigned long long)(nlive - 1);   // nlive arrivals in all
 }
@@ -835,9 +846,11 @@ __device__ void merge_group(const DecodeArgs& a, int b, int h, int nlive, uint8_
         const float* hp = stage + hh * nlive * kPartStride + 4 + d0;
         const float* w = sw + hh * kMaxSplits;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // a split with weight 0 adds exactly 0 (its stored values are finite:
+        // zeros when it saw no token), so the loop has no branch and unrolls
+#pragma unroll 4
         for (int sidx = 0; sidx < nlive; ++sidx) {
             const float ws = w[sidx];
-            if (ws == 0.0f) continue;
             if (G == 4) {
                 const float4 v = *reinterpret_cast<const float4*>(hp + sidx * kPartStride);
                 acc[0] = fmaf(ws, v.x, acc[0]);
@@ -1041,6 +1054,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
         const int q = warp - kFirstConsumer;
         griddep_wait();   // the packed query may come from the preceding grid
+        if (q == 0 && lane == 0) tag_counter(a, b, h);   // the consumer thread that counts this split in
         const uint8_t* qrec = a.qp ? a.qp + (size_t)b * a.qstride : smem + kQpOff;
         consume_pages<FMT, PM>(a, qrec, h, n, bt, smem, ctl, q, lane);   // contains (A)
         if (q == 0 && lane < 4) {   // no BF16 tokens in an FP4 split
