@@ -99,6 +99,7 @@ constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kSfaCol = 128;
 constexpr int kSfbSlots = 3;
+static_assert(kSfbSlots < kNK, "a K scale-factor slot's reuse waits on the K ring's empty phases");
 __device__ __forceinline__ uint32_t sfb_col(int slot, int j) { return 160u + 32u * slot + 16u * j; }
 constexpr int kN = 128;                          // MMA N: the page's tokens
 // The query operand: 28 core-matrix groups of 8 rows x 64 B, all zero but
@@ -112,7 +113,6 @@ struct alignas(16) Ctl {
     unsigned long long fullV[kNV], emptyV[kNV];   // V ring (empty: the page's consumer warp)
     unsigned long long accFull;                   // a round's scores are in the buffer
     unsigned long long accEmpty;                  // all four consumer warps have read the round
-    unsigned long long sfbFree[kSfbSlots];                // a K scale-factor slot's MMAs completed
     unsigned long long mmaDone;                   // every MMA the CTA issued has completed
     unsigned long long mergeBar;                  // the merging split's staged partials arrived
     float qred[kThreads / 32];                    // fused query: per-warp amax
@@ -122,6 +122,7 @@ struct alignas(16) Ctl {
     int last_split;                // this split completed its group's arrival count
     int nlive;                     // split 0 and the splits with pages of this (sequence, kv head)
     int tagK[kNK], tagV[kNV];      // page index each slot's latest fill holds (-1: none)
+    int okK[kNK];                  // the K slot's latest fill came from a pool page (published with its tag)
     uint32_t tmem;                 // TMEM base address
 };
 constexpr int kCtlBytes = (int)((sizeof(Ctl) + 127) / 128 * 128);
@@ -337,10 +338,12 @@ __device__ __forceinline__ void fill_slot(const DecodeArgs& a, int h, const int3
     const uint32_t full = smem_u32(isK ? &ctl->fullK[s] : &ctl->fullV[s]);
     uint8_t* slot = smem + (isK ? s : kNK + s) * kMaxRec;
     const int64_t phys = bt[k];
+    const bool ok = page_ok(phys, a.pool_pages);
+    if (isK) ctl->okK[s] = ok ? 1 : 0;   // read by the MMA lane once it has seen the tag
     // tag the fill before it is armed: consumers accept a completed phase
     // only together with their own page index
     st_release_shared(isK ? &ctl->tagK[s] : &ctl->tagV[s], k);
-    if (page_ok(phys, a.pool_pages)) {
+    if (ok) {
         const uint8_t* rec = a.pool + ((phys * a.hkv + h) * 2 + (isK ? 0 : 1)) * (int64_t)RB;
         mbar_arrive_expect_tx(full, RB);
         bulk_g2s_hint(smem_u32(slot), rec, RB, full, policy);
@@ -382,14 +385,19 @@ __device__ void mma_rounds(const DecodeArgs& a, int n, const int32_t* bt, uint8_
                 aborted = true;
                 break;
             }
-            // the scale-factor slot's previous MMAs (page k - kSfbSlots) have completed
-            if (k >= kSfbSlots && !mbar_wait_bounded(smem_u32(&ctl->sfbFree[slot]), ((k / kSfbSlots) - 1) & 1,
-                                                     kWaitLimitNs, &ctl->abort_flag)) {
-                aborted = true;
-                break;
+            // the scale-factor slot's previous MMAs (page k - kSfbSlots) have completed: the empty
+            // barrier of that page's K slot says so (its next phase needs the MMAs of page
+            // k - kSfbSlots + kNK > k, not issued yet, so the parity cannot alias)
+            if (k >= kSfbSlots) {
+                const int kp = k - kSfbSlots;
+                if (!mbar_wait_bounded(smem_u32(&ctl->emptyK[kp % kNK]), (kp / kNK) & 1, kWaitLimitNs,
+                                       &ctl->abort_flag)) {
+                    aborted = true;
+                    break;
+                }
             }
             tc_fence_after();
-            if (page_ok(bt[k], a.pool_pages)) {
+            if (ctl->okK[s]) {   // published by the producer with the tag wait_stage_page saw
                 const uint32_t ks = smem_u32(smem + s * kMaxRec);
                 for (int j = 0; j < kGroups; ++j) tmem_cp_sf(tm + sfb_col(slot, j), ks + kCodeBytes + 512 * j);
 #pragma unroll
@@ -409,11 +417,9 @@ __device__ void mma_rounds(const DecodeArgs& a, int n, const int32_t* bt, uint8_
                     }
                 }
                 first = false;
-                tc_commit(smem_u32(&ctl->sfbFree[slot]));
-                tc_commit(smem_u32(&ctl->emptyK[s]));
+                tc_commit(smem_u32(&ctl->emptyK[s]));   // frees the K slot and the scale-factor slot
             } else {
                 // an entry outside the pool: no data arrived, nothing to multiply
-                mbar_arrive(smem_u32(&ctl->sfbFree[slot]));
                 mbar_arrive(smem_u32(&ctl->emptyK[s]));
             }
         }
@@ -954,7 +960,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         }
         mbar_init(smem_u32(&ctl->accFull), 1);
         mbar_init(smem_u32(&ctl->accEmpty), kConsumers);
-        for (int s = 0; s < kSfbSlots; ++s) mbar_init(smem_u32(&ctl->sfbFree[s]), 1);
         mbar_init(smem_u32(&ctl->mmaDone), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();

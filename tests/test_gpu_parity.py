@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import nvfp4_kv_cache_bd_gb300 as bd
+from nvfp4_kv_cache_bd_gb300 import synth
 from tests import cases
 
 pytestmark = pytest.mark.gpu
@@ -199,11 +200,15 @@ def test_workspace_needs_no_initialization_and_is_reusable():
     read: one workspace that starts as garbage serves many calls, layers and
     batch shapes."""
     ctx = bd.Context(bd.make_config(num_layers=2))
+    shapes = ([16 + 128 * 20 + 5], [700, 16 + 128 * 9], [16 + 128 * 20 + 5])
+    # the size depends on the call's shape (its split layout), not only on B:
+    # one workspace shared by several shapes is sized for the largest need
     ws = None
-    for rep, lens in enumerate(([16 + 128 * 20 + 5], [700, 16 + 128 * 9], [16 + 128 * 20 + 5])):
+    for rep, lens in enumerate(shapes):
         c = cases.build(cases.Spec(lens=lens, seed=90 + rep), ctx=ctx)
-        need = bd.decode_workspace_size(ctx, 4, 64)
         if ws is None:
+            need = max(bd.decode_workspace_size(ctx, len(ls), max([1] + [synth.split_tokens(L)[1] for L in ls]))
+                       for ls in shapes)
             ws = torch.full((need // 4 + 1,), float("nan"), dtype=torch.float32, device="cuda")
         gpu = cases.run_gpu(c)
         ora = cases.run_oracle(c)
