@@ -87,7 +87,7 @@ constexpr int kLaunchRegs = 128, kCtlRegs = 40, kConsumerRegs = 2 * kLaunchRegs 
 static_assert(kCtlRegs % 8 == 0 && kConsumerRegs % 8 == 0 && kConsumerRegs <= 256, "setmaxnreg counts");
 constexpr int kRingBytes = (kNK + kNV) * kMaxRec;
 constexpr int kWavePages = 32;   // one-wave splits up to this many pages ...
-constexpr int kBatchPages = 16;  // ... else splits of this many (more if kMaxSplits needs it)
+constexpr int kBatchPages = 32;  // ... else splits of this many (more if kMaxSplits needs it)
 constexpr int kMaxSplits = 64;    // splits + 1 per (sequence, kv head)
 constexpr float kSmLog2e = 0.08838834764831845f * 1.4426950408889634f;  // log2(e)/sqrt(128)
 
