@@ -76,6 +76,14 @@ constexpr int kFirstConsumer = 4;
 constexpr int kThreads = 256;
 constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
 constexpr int kNK = 4, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
+// With the query quantized inside the decode, the rings are filled with the
+// first round's K and V records (kPreK, kPreV pages) before the wait for the
+// preceding grid, the rest after it: the later V pages would only queue, in
+// the memory system, ahead of the preceding grid's merge and this grid's
+// query load (128K step: 1222 against 1238 µs with all ten slots filled
+// first; with fewer K pages, 1232-1261).
+constexpr int kPreK = 4, kPreV = 4;
+static_assert(kPreK <= kNK && kPreV <= kNV, "pre-filled pages fit the rings");
 constexpr int kCtasPerSm = 2;
 // Register split of an FP4 split CTA: launched at kLaunchRegs per thread,
 // the control warpgroup gives registers back (setmaxnreg.dec to kCtlRegs)
@@ -981,14 +989,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     __syncthreads();
     tc_fence_after();
     if (!a.qp) {
-        // Fused query: the rings are empty, so the producers fill them now
-        // (the pages do not depend on the preceding grid); then the whole CTA
+        // Fused query: the rings are empty, so the producers fill the first
+        // round now (the pages do not depend on the preceding grid); then the whole CTA
         // quantizes this token's query into shared memory -- the bytes
         // bd_quantize_query writes -- one (head, 16-dim chunk) item a thread.
         if (warp < 2 && lane == 0) {
             const bool isK = (warp == 0);
             const uint64_t policy = l2_evict_first_policy();
-            for (int k = 0; k < min(n, isK ? kNK : kNV); ++k) fill_slot<FMT>(a, h, bt, smem, ctl, isK, k, policy);
+            for (int k = 0; k < min(n, isK ? kPreK : kPreV); ++k) fill_slot<FMT>(a, h, bt, smem, ctl, isK, k, policy);
         }
         __syncwarp();
         griddep_wait();   // q may come from the preceding grid
@@ -1026,8 +1034,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
             if (lane == 0) {
                 // each page is read once per call: evict it from L2 first
                 const uint64_t policy = l2_evict_first_policy();
-                // with the fused query the rings were filled before the roles split
-                for (int k = a.qp ? 0 : min(n, N); k < n; ++k) {
+                // with the fused query the first round was filled before the roles split
+                for (int k = a.qp ? 0 : min(n, isK ? kPreK : kPreV); k < n; ++k) {
                     const int s = k % N;
                     if (k >= N && !mbar_wait_bounded(smem_u32(&emptyb[s]), ((k / N) - 1) & 1, kWaitLimitNs,
                                                      &ctl->abort_flag)) {
