@@ -594,18 +594,43 @@ def main():
 # DRAM bytes (read + write) of one decode_kernel launch on the 131072-token
 # context, from ncu (dram__bytes_read.sum + dram__bytes_write.sum) on a 2-layer
 # run of this bench; a launch's traffic does not depend on the layer count.
-# Valid only for the kernel sources it was taken on: reported as null once
-# their hash differs.
-DECODE_TRAFFIC = {"sources_sha256_16": "e2fe4d34d7c5fc75", "ctx": 131072, "bytes": 151525376 + 3837696}
+# Valid only for the kernel code it was taken on: reported as null once the
+# hash of that code (comments and whitespace left out) differs.
+DECODE_TRAFFIC = {"sources_sha256_16": "7dcde84381ecaa17", "ctx": 131072, "bytes": 151525376 + 3837696}
 DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cuh")
+
+
+def code_only(src: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs folded to one
+    space: two sources with the same code_only text compile alike."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
 
 
 def decode_sources_hash():
     import hashlib
     h = hashlib.sha256()
     for f in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "nvfp4_kv_cache_bd_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "nvfp4_kv_cache_bd_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,12 +9,12 @@
 // tau in [0, 448]), RECIPE dual_residual_query_quantization (two query terms).
 //
 // Grid (nsplit + 1, kv heads, sequences) of 256-thread CTAs, two per SM; a
-// single-wave grid leaves a few SM slots free for the next layer's query
-// quantizer.  Split 0 of a (sequence, kv head) attends the BF16 sink and tail
+// single-wave grid leaves a few SM slots free, where the next layer's CTAs
+// start early.  Split 0 of a (sequence, kv head) attends the BF16 sink and tail
 // tokens with exact probabilities; split s >= 1 takes that sequence's FP4
 // pages [(s - 1) * pages_per_split, s * pages_per_split).  As this layer's
 // CTAs finish, the next layer's decode CTAs take their slots, so the next
-// decode's producers fill their rings during this one's tail.
+// decode's producers load its first round of pages during this one's tail.
 //
 // FP4 split CTA, two warpgroups with their own register shares:
 //  warp 0    streams the pages' K records, in page order, into a 4-slot
@@ -31,7 +31,7 @@
 //            round overwrites the buffer, the rest accumulate, and zero query
 //            rows leave the other quarters as they are);
 //  warp 3    owns the CTA's 256 TMEM columns (the score buffer, the query's
-//            and two pages' scale factors);
+//            scale factors and three pages' K scale factors);
 //  warps 4-7 consume: warp 4 + w takes page 4 r + w of every round alone.
 //            One tcgen05 load (16x256b) gives lane (g, t) the scores of query
 //            head g (both terms) for tokens 8 j + 2 t, 8 j + 2 t + 1 -- the
