@@ -37,7 +37,9 @@
  *  - bf16 tensors are raw 16-bit bfloat16 bit patterns (const void*).
  *  - The first launch call on a device allocates the context's device state
  *    (key-shift table, error word) with cudaMalloc; make that first call, or
- *    bd_set_key_shift(), before capturing a stream into a CUDA graph.
+ *    bd_set_key_shift(), before capturing a stream into a CUDA graph.  A
+ *    context then belongs to that device: a later call made while another
+ *    device is current returns BD_ERR_INVALID_ARG (one context per device).
  *
  * ---------------------------------------------------------------------------
  * Byte layouts (both the CUDA path and the independent CPU oracle write these)
