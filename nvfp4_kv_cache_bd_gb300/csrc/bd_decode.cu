@@ -163,13 +163,6 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ uint32_t lds16(const uint8_t* p) { return *reinterpret_cast<const uint16_t*>(p); }
 
-// f16 bits of 2^k for k <= 0 (subnormal below -14, zero below -24).
-__device__ __forceinline__ uint32_t f16_pow2(int k) {
-    if (k >= -14) return (uint32_t)(k + 15) << 10;
-    if (k >= -24) return 1u << (k + 24);
-    return 0u;
-}
-
 __device__ __forceinline__ int ld_acquire_shared(const int* p) {
     int v;
     asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
@@ -527,6 +520,10 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
     float o[8][4];
 #pragma unroll
     for (int bm = 0; bm < 8; ++bm) o[bm][0] = o[bm][1] = o[bm][2] = o[bm][3] = 0.0f;
+    // MXFP4: o holds O / 2^(ref - 127) for this lane's 32-dim V block: ref is
+    // the largest V scale byte of that block seen so far (-1: none yet), so
+    // every dequantized V value stays at most 6 in f16
+    int ref = -1;
 
     const int rounds = (n + 3) / 4;
     for (int r = 0; r < rounds; ++r) {
@@ -588,7 +585,7 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
         }
         l = fmaf(l, alpha, wpage * lp);
         const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcB);
-        if (FMT == BD_FORMAT_NVFP4) {
+        if (FMT == BD_FORMAT_NVFP4) {   // MXFP4: below, with the V reference
             if (__any_sync(kFull, (aA != 1.0f) | (aB != 1.0f))) {
 #pragma unroll
                 for (int bm = 0; bm < 8; ++bm) {
@@ -627,7 +624,7 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
                 ph[2 * i + 1] = hmul2(e2m1x2_to_f16x2(e2m1x2(__fmul_rn(u[2], inv), __fmul_rn(u[3], inv))), sdc);
             }
         }
-        if (FMT == BD_FORMAT_NVFP4) {
+        {
             // fold the page weight 2^(m_p - M) into Phat: P V accumulates straight into O
             const uint32_t wh = bcast_lo((uint32_t)__half_as_ushort(__float2half_rn(wpage)));
 #pragma unroll
@@ -641,12 +638,7 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
             break;
         }
         const uint8_t* Vs = smem + (kNK + sv) * kMaxRec;
-        float op[8][4];   // MXFP4: this page's O, merged below with the page's V reference exponent
-        float fv = 1.0f;
-        int ev_ref = 0;
         if (FMT == BD_FORMAT_MXFP4) {
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) op[bm][0] = op[bm][1] = op[bm][2] = op[bm][3] = 0.0f;
             int em = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -657,8 +649,23 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
             em = max(em, __shfl_xor_sync(kFull, em, 1));
             em = max(em, __shfl_xor_sync(kFull, em, 2));
             em = max(em, __shfl_xor_sync(kFull, em, 4));
-            ev_ref = em;
-            fv = pow2i(em - 127);
+            // a larger scale in this page raises the reference: o is scaled
+            // down by that exact power of two, together with the softmax
+            // rescale (a pass of no-op factors is skipped warp-wide)
+            const int nref = max(ref, em);
+            const int d = ref - nref;
+            const float rs = (ref < 0 || d == 0) ? 1.0f : (d < -126 ? 0.0f : pow2i(d));
+            ref = nref;
+            if (__any_sync(kFull, (aA != 1.0f) | (aB != 1.0f) | (rs != 1.0f))) {
+                const float fA = aA * rs, fB = aB * rs;
+#pragma unroll
+                for (int bm = 0; bm < 8; ++bm) {
+                    o[bm][0] *= fA;
+                    o[bm][1] *= fB;
+                    o[bm][2] *= fA;
+                    o[bm][3] *= fB;
+                }
+            }
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -675,8 +682,8 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
             } else {
                 const uint32_t e0 = lds16(Vs + kCodeBytes + ((i * 8 + t) * 4 + (g >> 1)) * 2);
                 const uint32_t e1 = lds16(Vs + kCodeBytes + ((i * 8 + t + 4) * 4 + (g >> 1)) * 2);
-                vs0 = f16_pow2((int)(e0 & 0xFF) - ev_ref) | (f16_pow2((int)(e0 >> 8) - ev_ref) << 16);
-                vs1 = f16_pow2((int)(e1 & 0xFF) - ev_ref) | (f16_pow2((int)(e1 >> 8) - ev_ref) << 16);
+                vs0 = f16x2_pow2((int)(e0 & 0xFF) - ref, (int)(e0 >> 8) - ref);
+                vs1 = f16x2_pow2((int)(e1 & 0xFF) - ref, (int)(e1 >> 8) - ref);
             }
             const uint32_t b01 = ph[2 * i], b23 = ph[2 * i + 1];
             const uint32_t vw0[4] = {v0.x, v0.y, v0.z, v0.w}, vw1[4] = {v1.x, v1.y, v1.z, v1.w};
@@ -691,40 +698,32 @@ __device__ void consume_pages(const DecodeArgs& a, const uint8_t* qrec, int h, i
                 A[1] = hmul2(f0[1], vs0);
                 A[2] = hmul2(f1[0], vs1);
                 A[3] = hmul2(f1[1], vs1);
-                mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j] : op[2 * j], A, b01, b23);
+                mma16816(o[2 * j], A, b01, b23);
                 A[0] = hmul2(f0[2], vs0);
                 A[1] = hmul2(f0[3], vs0);
                 A[2] = hmul2(f1[2], vs1);
                 A[3] = hmul2(f1[3], vs1);
-                mma16816(FMT == BD_FORMAT_NVFP4 ? o[2 * j + 1] : op[2 * j + 1], A, b01, b23);
+                mma16816(o[2 * j + 1], A, b01, b23);
             }
         }
         // release the V slot: every lane's shared-memory reads are done
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&ctl->emptyV[sv]));
-        if (FMT == BD_FORMAT_MXFP4) {
-            const float bA = __shfl_sync(kFull, wpage, srcA) * fv, bB = __shfl_sync(kFull, wpage, srcB) * fv;
-#pragma unroll
-            for (int bm = 0; bm < 8; ++bm) {
-                o[bm][0] = fmaf(o[bm][0], aA, bA * op[bm][0]);
-                o[bm][1] = fmaf(o[bm][1], aB, bB * op[bm][1]);
-                o[bm][2] = fmaf(o[bm][2], aA, bA * op[bm][2]);
-                o[bm][3] = fmaf(o[bm][3], aB, bB * op[bm][3]);
-            }
-        }
     }
 
     // ---------------- hand the warp state to the CTA merge
     __syncthreads();   // (A) the ring and every MMA are done with
     float* sO = reinterpret_cast<float*>(smem);   // [consumer warps][4 heads][128]
+    // NVFP4: the per-tensor V scale; MXFP4: the lane's reference 2^(ref - 127)
+    const float gout = (FMT == BD_FORMAT_NVFP4) ? gV : (ref < 0 ? 0.0f : pow2i(ref - 127));
     if (t < 2) {
 #pragma unroll
         for (int bm = 0; bm < 8; ++bm) {
             const int d = 16 * g + 2 * bm;
-            sO[(w * 4 + 2 * t) * kD + d] = o[bm][0] * gV;
-            sO[(w * 4 + 2 * t + 1) * kD + d] = o[bm][1] * gV;
-            sO[(w * 4 + 2 * t) * kD + d + 1] = o[bm][2] * gV;
-            sO[(w * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3] * gV;
+            sO[(w * 4 + 2 * t) * kD + d] = o[bm][0] * gout;
+            sO[(w * 4 + 2 * t + 1) * kD + d] = o[bm][1] * gout;
+            sO[(w * 4 + 2 * t) * kD + d + 1] = o[bm][2] * gout;
+            sO[(w * 4 + 2 * t + 1) * kD + d + 1] = o[bm][3] * gout;
         }
     }
     l += __shfl_xor_sync(kFull, l, 1);

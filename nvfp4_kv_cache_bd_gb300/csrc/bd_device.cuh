@@ -125,6 +125,24 @@ __device__ __forceinline__ uint32_t e4m3_div6(float a) {
 
 // ------------------------------------------------------------- f16x2 math --
 
+// f16x2 of (2^klo, 2^khi) for k <= 0, by one conversion: 2^k is exact in
+// binary32 down to 2^-126 (lower k clamped there), and its round-to-nearest
+// f16 is 2^k itself down to 2^-24, 0 below (2^-25 is a tie, to the even 0) --
+// the values f16_pow2 builds bit by bit.
+__device__ __forceinline__ uint32_t f16x2_pow2(int klo, int khi) {
+    const float lo = __uint_as_float((uint32_t)(max(klo, -126) + 127) << 23);
+    const float hi = __uint_as_float((uint32_t)(max(khi, -126) + 127) << 23);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// f16 bits of 2^k for k <= 0 (subnormal below -14, zero below -24).
+__device__ __forceinline__ uint32_t f16_pow2(int k) {
+    if (k >= -14) return (uint32_t)(k + 15) << 10;
+    if (k >= -24) return 1u << (k + 24);
+    return 0u;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
