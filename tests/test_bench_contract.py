@@ -47,3 +47,17 @@ def test_reference_arm_is_silent_on_other_ranks():
     r = run_bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_traffic_record_hash_ignores_comments_and_whitespace():
+    """The measured-traffic record follows the decode sources' code only:
+    comments and whitespace runs leave the hash alone, anything else (string
+    contents included) changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    code = 'int a = 1; /* block */ const char* s = "x // y";  // line\nfloat b;'
+    assert bench.code_only(code) == 'int a = 1; const char* s = "x // y"; float b;'
+    assert bench.code_only("a\n\n   b // c\n") == bench.code_only("a b")
+    assert bench.code_only('s = "/* kept */";') == 's = "/* kept */";'
+    assert bench.code_only("x = 1;") != bench.code_only("x = 2;")
+    assert len(bench.decode_sources_hash()) == 16
