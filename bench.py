@@ -64,6 +64,17 @@ def parse():
     return ap.parse_args()
 
 
+def sm_max_mhz():
+    """The maximum SM clock measured on this machine (MEASURED_PEAKS.json), else
+    the GB300's nominal 2070 MHz."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if d.get("sm_max_mhz"):
+            return float(d["sm_max_mhz"])
+    return 2070.0
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -598,6 +609,11 @@ def main():
 # hash of that code (comments and whitespace left out) differs.
 DECODE_TRAFFIC = {"sources_sha256_16": "855c128f222e9286", "ctx": 131072, "bytes": 151524352 + 3700480}
 DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cuh")
+# Warp instructions one NVFP4 writer launch of the writer bench executes
+# (ncu smsp__inst_executed.sum, profiles/writer_kernel_64seq_page_fill.md),
+# for the writer's issue-rate roofline; null once its code changes.
+WRITER_INSTR = {"sources_sha256_16": "910f333b26f12645", "fmt": 0, "warp_instructions": 14311424}
+WRITER_SOURCES = ("bd_writer.cu", "bd_device.cuh", "bd_internal.h")
 
 
 def code_only(src: str) -> str:
@@ -625,13 +641,17 @@ def code_only(src: str) -> str:
     return " ".join("".join(out).split())
 
 
-def decode_sources_hash():
+def sources_hash(files):
     import hashlib
     h = hashlib.sha256()
-    for f in DECODE_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "nvfp4_kv_cache_bd_gb300", "csrc", f), encoding="utf-8") as fh:
             h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
+
+
+def decode_sources_hash():
+    return sources_hash(DECODE_SOURCES)
 
 
 def decode_traffic(args):
@@ -758,12 +778,27 @@ def bench_writer(args, device, stream, torch, bd, pg, hbm_peak, fmt=0, clocks=No
     call_ms = statistics.mean(durs)
     tok = seqs * 128
     fmt_name = "NVFP4" if fmt == 0 else "MXFP4"
-    return {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, {fmt_name}",
-            "tok_per_s": job_rate(tok, ms, pg.get_world_size() if pg is not None else 1),
-            "ms_per_step": ms, "gpu_launches_per_step": layers,
-            "roofline": {"bound": "hbm", "kernel": "writer_kernel", "achieved": call_bytes / (call_ms * 1e-3) / 1e9,
-                         "peak": hbm_peak, "unit": "GB/s", "frac": call_bytes / (call_ms * 1e-3) / 1e9 / hbm_peak,
-                         "bytes_per_launch": call_bytes}}
+    out = {"workload": f"{seqs} seqs x {layers} layers x 8 kv heads, one 128-token page of K and V each, {fmt_name}",
+           "tok_per_s": job_rate(tok, ms, pg.get_world_size() if pg is not None else 1),
+           "ms_per_step": ms, "gpu_launches_per_step": layers,
+           "roofline": {"bound": "hbm", "kernel": "writer_kernel", "achieved": call_bytes / (call_ms * 1e-3) / 1e9,
+                        "peak": hbm_peak, "unit": "GB/s", "frac": call_bytes / (call_ms * 1e-3) / 1e9 / hbm_peak,
+                        "bytes_per_launch": call_bytes}}
+    # The writer is bound by instruction issue, not by HBM: the same launch
+    # against the SMs' issue rate (one warp instruction per scheduler and
+    # cycle: SMs x 4 x the maximum SM clock), on its in-step duration.
+    if fmt == WRITER_INSTR["fmt"] and sources_hash(WRITER_SOURCES) == WRITER_INSTR["sources_sha256_16"]:
+        props = torch.cuda.get_device_properties(device)
+        mhz = sm_max_mhz()
+        peak = props.multi_processor_count * 4 * mhz * 1e6 / 1e12
+        step_launch_s = ms * 1e-3 / layers
+        ach = WRITER_INSTR["warp_instructions"] / step_launch_s / 1e12
+        out["roofline_issue"] = {"bound": "alu", "kernel": "writer_kernel", "achieved": ach, "peak": peak,
+                                 "unit": "T warp instructions/s", "frac": ach / peak,
+                                 "warp_instructions_per_launch": WRITER_INSTR["warp_instructions"],
+                                 "basis": f"{props.multi_processor_count} SMs x 4 schedulers x {mhz:.0f} MHz; "
+                                          "in-step launch time (step / layers)"}
+    return out
 
 
 if __name__ == "__main__":
