@@ -612,7 +612,7 @@ DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cu
 # Warp instructions one NVFP4 writer launch of the writer bench executes
 # (ncu smsp__inst_executed.sum, profiles/writer_kernel_64seq_page_fill.md),
 # for the writer's issue-rate roofline; null once its code changes.
-WRITER_INSTR = {"sources_sha256_16": "910f333b26f12645", "fmt": 0, "warp_instructions": 14311424}
+WRITER_INSTR = {"sources_sha256_16": "345cadbc6fabd91d", "fmt": 0, "warp_instructions": 10993664}
 WRITER_SOURCES = ("bd_writer.cu", "bd_device.cuh", "bd_internal.h")
 
 

@@ -31,6 +31,10 @@ struct WriterArgs {
     int n, hkv, format, key_search, rotation, centering;
     int pool_pages;           // 0: only negative destination pages are rejected
     float gk, gv;
+    // -0.0f, read by the kernel at run time: the addend of the fma that forms
+    // a product which is summed later, so that the compiler cannot see the
+    // addend is zero and fold the product into the sum (x*y + -0 = RN(x*y)).
+    float zero_addend = -0.0f;
     // Append mode (bd_append_kv) when seq_lens is set: n = B sequences, k/v
     // are the BF16 tail buffers [B][128][Hkv][128]; the new token is stored
     // at position seq_lens[b] and the tail page it completes is packed into

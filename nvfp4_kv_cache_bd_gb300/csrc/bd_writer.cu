@@ -20,10 +20,10 @@
 //    chunk c = lane/8), so both nibbles of a V code byte are produced in the
 //    same lane and the 16-token tile is written with 16-byte stores.
 // Every rounding step is the IEEE binary32 operation the oracle performs
-// (explicit __f*_rn intrinsics, so nothing is contracted into an FMA; the
-// one FMA, in the cross-lane butterflies, multiplies by +-1 and rounds once
-// like the add it replaces); the E2M1 / E4M3 encodings come from the
-// sm_100-family cvt instructions.
+// (explicit __f*_rn intrinsics, scalar or two-lane packed, so nothing is
+// contracted into an FMA; the FMAs that are written out multiply by +-1 and
+// round once like the add or subtract they replace); the E2M1 / E4M3
+// encodings come from the sm_100-family cvt instructions.
 #include "bd_device.cuh"
 
 namespace bd {
@@ -82,50 +82,99 @@ __device__ __forceinline__ uint32_t e2m1x2_enc_dec(float lo, float hi, uint32_t&
     return byte;
 }
 
-// Squared-error tree over 16 terms: w[i] += w[i+8], then +4, +2, +1.
-__device__ __forceinline__ float tree16(float* w) {
-#pragma unroll
-    for (int h = 8; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[i], w[i + h]);
-    return w[0];
-}
+// Two-lane binary32 arithmetic: one packed instruction, each lane rounded to
+// nearest like the scalar add, subtract, multiply or fma.  The compiler has
+// been seen to fuse a packed multiply into a packed add or subtract that
+// consumes it (one rounding instead of two), .rn notwithstanding.  So every
+// product that is summed later is formed as fma(x, y, z) with z = -0.0f read
+// at run time (mulz2): exactly RN(x*y), and no single instruction can take
+// its place together with the sum.  Products that only feed a conversion or
+// another product stay plain multiplies (mul2).
+#define BD_F32X2_OP(name, op)                                                                      \
+    __device__ __forceinline__ float2 name(float2 a, float2 b) {                                   \
+        float2 r;                                                                                  \
+        asm("{\n\t.reg .b64 ra, rb, rr;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t" \
+            op " rr, ra, rb;\n\tmov.b64 {%0, %1}, rr;\n\t}"                                     \
+            : "=f"(r.x), "=f"(r.y)                                                                 \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                             \
+        return r;                                                                                  \
+    }
+BD_F32X2_OP(add2, "add.rn.f32x2")
+BD_F32X2_OP(sub2, "sub.rn.f32x2")
+BD_F32X2_OP(mul2, "mul.rn.f32x2")
+#undef BD_F32X2_OP
 
-// Encode 16 values with scale (S, inv) into 8 code bytes (w0: elements 0-7,
-// w1: 8-15) and fill w[] with squared reconstruction errors.
+// a * b + c per lane, rounded once.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n\t.reg .b64 ra, rb, rc, rr;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rr, ra, rb, rc;\n\tmov.b64 {%0, %1}, rr;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+// a * b rounded once, for a product that a later add or subtract consumes;
+// z holds the run-time -0.0f (WriterArgs::zero_addend) in both lanes.
+__device__ __forceinline__ float2 mulz2(float2 a, float2 b, float2 z) { return fma2(a, b, z); }
+
+// Encode 8 pairs (elements 2i, 2i+1 in xp[i]) with scale (S, inv) into 8
+// code bytes (w0: elements 0-7, w1: 8-15) and fill wp[] with the squared
+// reconstruction errors of the same pairs.  A zero block encodes with
+// inv = 0 and has its codes cleared afterwards: its x_hat is +-0 * S = +-0,
+// so its errors are x^2 as for the decoded zero codes.
 template <bool kErr>
-__device__ __forceinline__ void enc16(const float* x, float S, float inv, bool zero, uint32_t& w0,
-                                      uint32_t& w1, float* w) {
+__device__ __forceinline__ void enc16x2(const float2* xp, float S, float inv, bool zero, float2 z, uint32_t& w0,
+                                        uint32_t& w1, float2* wp) {
+    const float2 inv2 = splat2(zero ? 0.0f : inv), S2 = splat2(S);
     w0 = 0;
     w1 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        uint32_t byte = 0, hv = 0;
-        if (!zero) byte = e2m1x2_enc_dec(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv), hv);
+        uint32_t hv;
+        const float2 q = mul2(xp[i], inv2);
+        const uint32_t byte = e2m1x2_enc_dec(q.x, q.y, hv);
         if (i < 4) w0 |= byte << (8 * i);
         else w1 |= byte << (8 * (i - 4));
         if (kErr) {
-            // a zero block decodes to 0 and S is finite, so x_hat = 0 * S = +0
-            const float2 val = f16x2_to_float2(hv);
-            const float e0 = __fsub_rn(x[2 * i], __fmul_rn(val.x, S));
-            const float e1 = __fsub_rn(x[2 * i + 1], __fmul_rn(val.y, S));
-            w[2 * i] = __fmul_rn(e0, e0);
-            w[2 * i + 1] = __fmul_rn(e1, e1);
+            const float2 e = sub2(xp[i], mulz2(f16x2_to_float2(hv), S2, z));
+            wp[i] = mulz2(e, e, z);
         }
+    }
+    if (zero) {
+        w0 = 0;
+        w1 = 0;
     }
 }
 
-__device__ __forceinline__ float amax_of(const float* x, int n) {
-    float a = 0.0f;
-    for (int i = 0; i < n; ++i) a = fmaxf(a, fabsf(x[i]));
-    return a;
+// Squared-error tree over 16 terms w[i] += w[i+8], then +4, +2, +1, with the
+// terms held as pairs wp[i] = (w[2i], w[2i+1]): two additions per
+// instruction until the last.
+__device__ __forceinline__ float tree16x2(float2* wp) {
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) wp[i] = add2(wp[i], wp[i + h]);
+    return __fadd_rn(wp[0].x, wp[0].y);
 }
 
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* x) {
-    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
-    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
-    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+// The 8 code bytes of the 8 pairs quantized with exponent e (w0: elements
+// 0-7, w1: 8-15) and their squared errors.
+__device__ __forceinline__ void mx_enc_err16x2(const float2* xp, int e, float2 z, uint32_t& w0, uint32_t& w1,
+                                               float2* wp) {
+    const float2 down = splat2(pow2i(-e)), up = splat2(pow2i(e));
+    w0 = 0;
+    w1 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t hv;
+        const float2 q = mul2(xp[i], down);
+        const uint32_t byte = e2m1x2_enc_dec(q.x, q.y, hv);
+        if (i < 4) w0 |= byte << (8 * i);
+        else w1 |= byte << (8 * (i - 4));
+        const float2 err = sub2(xp[i], mulz2(f16x2_to_float2(hv), up, z));
+        wp[i] = mulz2(err, err, z);
+    }
 }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
@@ -139,83 +188,91 @@ __device__ __forceinline__ void mx_candidates(float amax, int& ea, int& eb) {
     eb = min(127, max(-127, E - 1));
 }
 
-// Squared errors of 16 values quantized with exponent e.
-__device__ __forceinline__ void mx_err16(const float* x, int e, float* w) {
-    float down = pow2i(-e), up = pow2i(e);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t byte = e2m1x2(__fmul_rn(x[2 * i], down), __fmul_rn(x[2 * i + 1], down));
-        float2 val = f16x2_to_float2(e2m1x2_to_f16x2(byte));
-        float e0 = __fsub_rn(x[2 * i], __fmul_rn(val.x, up));
-        float e1 = __fsub_rn(x[2 * i + 1], __fmul_rn(val.y, up));
-        w[2 * i] = __fmul_rn(e0, e0);
-        w[2 * i + 1] = __fmul_rn(e1, e1);
-    }
-}
-
 // ------------------------------------------------------------------ K tile --
 
+// bf16 x 8 -> four pairs (elements 2i, 2i+1 in xp[i]).
+__device__ __forceinline__ void unpack_bf16x8_2(const uint4& u, float2* xp) {
+    xp[0] = make_float2(bf16_lo(u.x), bf16_hi(u.x));
+    xp[1] = make_float2(bf16_lo(u.y), bf16_hi(u.y));
+    xp[2] = make_float2(bf16_lo(u.z), bf16_hi(u.z));
+    xp[3] = make_float2(bf16_lo(u.w), bf16_hi(u.w));
+}
+
+// A lane's 16 dims are held as 8 pairs xp[i] = (x[2i], x[2i+1]); every step
+// below is the scalar sequence of the transform and the search, two
+// elements per packed instruction where both take the same operation.
 template <int FMT>
 __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, int row0, const float* stab, uint8_t* rec,
                              int grp, int lane, int h) {
     const int r = lane >> 3, c = lane & 7;
-    float mu[16];
+    const float2 z = splat2(a.zero_addend);
+    float2 mu[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mu[i] = (a.centering && a.mu) ? a.mu[h * kD + 16 * c + i] : 0.0f;
+    for (int i = 0; i < 8; ++i)
+        mu[i] = (a.centering && a.mu) ? make_float2(a.mu[h * kD + 16 * c + 2 * i], a.mu[h * kD + 16 * c + 2 * i + 1])
+                                      : make_float2(0.0f, 0.0f);
 
 #pragma unroll 1
     for (int j = 0; j < 4; ++j) {
         const int tok = 16 * grp + 4 * j + r;
-        float x[16];
-        unpack_bf16x8(lds128(tile + (tok - row0) * kTilePitch + 32 * c), x);
-        unpack_bf16x8(lds128(tile + (tok - row0) * kTilePitch + 32 * c + 16), x + 8);
+        float2 xp[8];
+        unpack_bf16x8_2(lds128(tile + (tok - row0) * kTilePitch + 32 * c), xp);
+        unpack_bf16x8_2(lds128(tile + (tok - row0) * kTilePitch + 32 * c + 16), xp + 4);
         if (a.centering) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __fsub_rn(x[i], mu[i]);
+            for (int i = 0; i < 8; ++i) xp[i] = sub2(xp[i], mu[i]);
         }
         if (a.rotation) {
-            // strides 1, 2, 4, 8 inside the lane
+            // stride 1 inside each pair
 #pragma unroll
-            for (int hs = 1; hs < 16; hs <<= 1)
+            for (int i = 0; i < 8; ++i) {
+                const float u = xp[i].x, v = xp[i].y;
+                xp[i] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
+            }
+            // strides 2, 4, 8 between pairs
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
+            for (int hs = 1; hs < 8; hs <<= 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
                     if (!(i & hs)) {
-                        float u = x[i], v = x[i + hs];
-                        x[i] = __fadd_rn(u, v);
-                        x[i + hs] = __fsub_rn(u, v);
+                        const float2 u = xp[i], v = xp[i + hs];
+                        xp[i] = add2(u, v);
+                        xp[i + hs] = sub2(u, v);
                     }
             // strides 16, 32, 64 across lanes c^1, c^2, c^4
 #pragma unroll
             for (int m = 1; m <= 4; m <<= 1) {
                 // p - x in the upper lane, x + p in the lower one: fma(x, +-1, p)
                 // rounds the exact p +- x once, like the add or subtract
-                const float sgn = (c & m) ? -1.0f : 1.0f;
+                const float2 sgn = splat2((c & m) ? -1.0f : 1.0f);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p = __shfl_xor_sync(kFull, x[i], m);
-                    x[i] = __fmaf_rn(x[i], sgn, p);
+                for (int i = 0; i < 8; ++i) {
+                    const float2 p = make_float2(__shfl_xor_sync(kFull, xp[i].x, m), __shfl_xor_sync(kFull, xp[i].y, m));
+                    xp[i] = fma2(xp[i], sgn, p);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], kRot);
+            for (int i = 0; i < 8; ++i) xp[i] = mulz2(xp[i], splat2(kRot), z);
         }
 
         uint32_t w0, w1, sb;
-        float w[16];
-        const float amax = amax_of(x, 16);
+        float2 wp[8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(xp[i].x), fabsf(xp[i].y)));
         if (FMT == BD_FORMAT_NVFP4) {
             Scale s6 = nv_scale(amax, 6.0f, a.gk, stab);
             if (a.key_search) {
                 uint32_t c0, c1;
-                enc16<true>(x, s6.S, s6.inv, s6.zero, c0, c1, w);
-                const float e6 = tree16(w);
+                enc16x2<true>(xp, s6.S, s6.inv, s6.zero, z, c0, c1, wp);
+                const float e6 = tree16x2(wp);
                 Scale s4 = nv_scale(amax, 4.0f, a.gk, stab);
-                enc16<true>(x, s4.S, s4.inv, s4.zero, w0, w1, w);
-                const float e4 = tree16(w);
+                enc16x2<true>(xp, s4.S, s4.inv, s4.zero, z, w0, w1, wp);
+                const float e4 = tree16x2(wp);
                 sb = s4.sb;
                 if (!(e4 < e6)) { w0 = c0; w1 = c1; sb = s6.sb; }
             } else {
-                enc16<false>(x, s6.S, s6.inv, s6.zero, w0, w1, w);
+                enc16x2<false>(xp, s6.S, s6.inv, s6.zero, z, w0, w1, wp);
                 sb = s6.sb;
             }
         } else {
@@ -224,17 +281,21 @@ __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, int row0,
             const float amax32 = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
             int ea, eb;
             mx_candidates(amax32 == 0.0f ? 1.0f : amax32, ea, eb);
-            mx_err16(x, ea, w);
+            uint32_t c0, c1;
+            mx_enc_err16x2(xp, ea, z, c0, c1, wp);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __fadd_rn(w[i], __shfl_xor_sync(kFull, w[i], 1));
-            const float sa = tree16(w);
-            mx_err16(x, eb, w);
+            for (int i = 0; i < 8; ++i)
+                wp[i] = add2(wp[i], make_float2(__shfl_xor_sync(kFull, wp[i].x, 1), __shfl_xor_sync(kFull, wp[i].y, 1)));
+            const float sa = tree16x2(wp);
+            mx_enc_err16x2(xp, eb, z, w0, w1, wp);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __fadd_rn(w[i], __shfl_xor_sync(kFull, w[i], 1));
-            const float sbb = tree16(w);
+            for (int i = 0; i < 8; ++i)
+                wp[i] = add2(wp[i], make_float2(__shfl_xor_sync(kFull, wp[i].x, 1), __shfl_xor_sync(kFull, wp[i].y, 1)));
+            const float sbb = tree16x2(wp);
+            // the codes of the chosen candidate; a zero block has codes 0
             const int e = (amax32 == 0.0f) ? -127 : ((sbb < sa) ? eb : ea);
-            const float down = pow2i(-e);
-            enc16<false>(x, 0.0f, down, amax32 == 0.0f, w0, w1, w);
+            if (!(sbb < sa)) { w0 = c0; w1 = c1; }
+            if (amax32 == 0.0f) { w0 = 0; w1 = 0; }
             sb = (amax32 == 0.0f) ? 0u : (uint32_t)(e + 127);
         }
         // codes in groups of 8 tokens x 32 dims (128 B each); scale byte of
@@ -249,40 +310,67 @@ __device__ void write_k_tile(const WriterArgs& a, const uint8_t* tile, int row0,
 
 // ------------------------------------------------------------------ V tile --
 
-// Encode the same 16 dims of two tokens into 16 paired code bytes.
-__device__ __forceinline__ void enc_pair16(const float* x0, const float* x1, float inv0, bool z0, float inv1,
-                                           bool z1, uint32_t* words) {
+// bf16 x 8 of two tokens -> eight (token 0, token 1) pairs of the same dims.
+__device__ __forceinline__ void unpack_rows_2(const uint4& u0, const uint4& u1, float2* xv) {
+    xv[0] = make_float2(bf16_lo(u0.x), bf16_lo(u1.x));
+    xv[1] = make_float2(bf16_hi(u0.x), bf16_hi(u1.x));
+    xv[2] = make_float2(bf16_lo(u0.y), bf16_lo(u1.y));
+    xv[3] = make_float2(bf16_hi(u0.y), bf16_hi(u1.y));
+    xv[4] = make_float2(bf16_lo(u0.z), bf16_lo(u1.z));
+    xv[5] = make_float2(bf16_hi(u0.z), bf16_hi(u1.z));
+    xv[6] = make_float2(bf16_lo(u0.w), bf16_lo(u1.w));
+    xv[7] = make_float2(bf16_hi(u0.w), bf16_hi(u1.w));
+}
+
+// Encode 16 dims of two tokens (xv[d] = (token 0, token 1)) into 16 paired
+// code bytes, token 0 in the low nibble: inv holds each token's 1/S.
+__device__ __forceinline__ void enc_pairs16(const float2* xv, float2 inv, uint32_t* words) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t wd = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const int d = 4 * q + b;
-            const float lo = z0 ? 0.0f : __fmul_rn(x0[d], inv0);
-            const float hi = z1 ? 0.0f : __fmul_rn(x1[d], inv1);
-            wd |= e2m1x2(lo, hi) << (8 * b);
+            const float2 v = mul2(xv[4 * q + b], inv);
+            wd |= e2m1x2(v.x, v.y) << (8 * b);
         }
         words[q] = wd;
     }
 }
 
-__device__ __forceinline__ int mx_search32(const float* x) {
-    const float amax = amax_of(x, 32);
-    if (amax == 0.0f) return -128;   // marker: zero block
-    int ea, eb;
-    mx_candidates(amax, ea, eb);
-    float w[16], w2[16];
-    mx_err16(x, ea, w);
-    mx_err16(x + 16, ea, w2);
+// Code-word mask that clears the nibbles of zero blocks (token 0's are the
+// low nibbles): their codes are 0, whatever the sign of the encoded zeros.
+__device__ __forceinline__ uint32_t zero_mask(bool z0, bool z1) {
+    return (z0 ? 0xF0F0F0F0u : 0xFFFFFFFFu) & (z1 ? 0x0F0F0F0Fu : 0xFFFFFFFFu);
+}
+
+// One MXFP4 candidate for the 32-dim blocks of two tokens at once, exponent
+// e.x for token 0 and e.y for token 1: the 32 paired code bytes and both
+// squared-error sums, each summed as w[i] = err(i) + err(16+i), then the
+// tree levels w[i] += w[i+8], +4, +2, +1.
+__device__ __forceinline__ float2 mx_pair_cand32(const float2* xv, int e0, int e1, float2 z, uint32_t* words) {
+    const float2 down = make_float2(pow2i(-e0), pow2i(-e1)), up = make_float2(pow2i(e0), pow2i(e1));
+    float2 w[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = __fadd_rn(w[i], w2[i]);
-    const float sa = tree16(w);
-    mx_err16(x, eb, w);
-    mx_err16(x + 16, eb, w2);
+    for (int q = 0; q < 8; ++q) words[q] = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = __fadd_rn(w[i], w2[i]);
-    const float sbb = tree16(w);
-    return (sbb < sa) ? eb : ea;
+    for (int i = 0; i < 8; ++i) {
+        float2 t[4];   // dims i, 16+i, 8+i, 24+i
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = i + (k == 1 ? 16 : k == 2 ? 8 : k == 3 ? 24 : 0);
+            uint32_t hv;
+            const float2 v = mul2(xv[d], down);
+            words[d >> 2] |= e2m1x2_enc_dec(v.x, v.y, hv) << (8 * (d & 3));
+            const float2 err = sub2(xv[d], mulz2(f16x2_to_float2(hv), up, z));
+            t[k] = mulz2(err, err, z);
+        }
+        w[i] = add2(add2(t[0], t[1]), add2(t[2], t[3]));
+    }
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i) w[i] = add2(w[i], w[i + h]);
+    return w[0];
 }
 
 template <int FMT>
@@ -301,31 +389,49 @@ __device__ void write_v_tile(const WriterArgs& a, const uint8_t* tile, int row0,
         uint32_t sbs = 0;
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-            float x0[16], x1[16];
-            unpack_bf16x8(lds128(r0 + 32 * blk), x0);
-            unpack_bf16x8(lds128(r0 + 32 * blk + 16), x0 + 8);
-            unpack_bf16x8(lds128(r1 + 32 * blk), x1);
-            unpack_bf16x8(lds128(r1 + 32 * blk + 16), x1 + 8);
-            Scale s0 = nv_scale(amax_of(x0, 16), 6.0f, a.gv, stab);
-            Scale s1 = nv_scale(amax_of(x1, 16), 6.0f, a.gv, stab);
-            enc_pair16(x0, x1, s0.inv, s0.zero, s1.inv, s1.zero, words + 4 * blk);
+            float2 xv[16];
+            unpack_rows_2(lds128(r0 + 32 * blk), lds128(r1 + 32 * blk), xv);
+            unpack_rows_2(lds128(r0 + 32 * blk + 16), lds128(r1 + 32 * blk + 16), xv + 8);
+            float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+            for (int d = 0; d < 16; ++d) {
+                am0 = fmaxf(am0, fabsf(xv[d].x));
+                am1 = fmaxf(am1, fabsf(xv[d].y));
+            }
+            Scale s0 = nv_scale(am0, 6.0f, a.gv, stab);
+            Scale s1 = nv_scale(am1, 6.0f, a.gv, stab);
+            enc_pairs16(xv, make_float2(s0.zero ? 0.0f : s0.inv, s1.zero ? 0.0f : s1.inv), words + 4 * blk);
+            const uint32_t m = zero_mask(s0.zero, s1.zero);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) words[4 * blk + q] &= m;
             sbs |= (s0.sb | (s1.sb << 8)) << (16 * blk);
         }
         *reinterpret_cast<uint32_t*>(rec + kCodeBytes + ((grp * 8 + p) * 8 + 2 * c) * 2) = sbs;
     } else {
-        float x0[32], x1[32];
+        float2 xv[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            unpack_bf16x8(lds128(r0 + 16 * k), x0 + 8 * k);
-            unpack_bf16x8(lds128(r1 + 16 * k), x1 + 8 * k);
+        for (int k = 0; k < 4; ++k) unpack_rows_2(lds128(r0 + 16 * k), lds128(r1 + 16 * k), xv + 8 * k);
+        float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+        for (int d = 0; d < 32; ++d) {
+            am0 = fmaxf(am0, fabsf(xv[d].x));
+            am1 = fmaxf(am1, fabsf(xv[d].y));
         }
-        const int e0 = mx_search32(x0), e1 = mx_search32(x1);
-        const bool z0 = e0 == -128, z1 = e1 == -128;
-        const float d0 = z0 ? 0.0f : pow2i(-e0), d1 = z1 ? 0.0f : pow2i(-e1);
-        enc_pair16(x0, x1, d0, z0, d1, z1, words);
-        enc_pair16(x0 + 16, x1 + 16, d0, z0, d1, z1, words + 4);
-        const uint32_t b0 = z0 ? 0u : (uint32_t)(e0 + 127), b1 = z1 ? 0u : (uint32_t)(e1 + 127);
-        *reinterpret_cast<uint16_t*>(rec + kCodeBytes + ((grp * 8 + p) * 4 + c) * 2) = (uint16_t)(b0 | (b1 << 8));
+        const bool z0 = am0 == 0.0f, z1 = am1 == 0.0f;   // zero blocks: codes 0, scale byte 0
+        int ea0, eb0, ea1, eb1;
+        mx_candidates(z0 ? 1.0f : am0, ea0, eb0);
+        mx_candidates(z1 ? 1.0f : am1, ea1, eb1);
+        uint32_t wb[8];
+        const float2 z = splat2(a.zero_addend);
+        const float2 sa = mx_pair_cand32(xv, ea0, ea1, z, words);
+        const float2 sbb = mx_pair_cand32(xv, eb0, eb1, z, wb);
+        const bool b0 = sbb.x < sa.x, b1 = sbb.y < sa.y;   // the larger exponent only when strictly better
+        const uint32_t mb = (b0 ? 0x0F0F0F0Fu : 0u) | (b1 ? 0xF0F0F0F0u : 0u), mz = zero_mask(z0, z1);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) words[q] = ((words[q] & ~mb) | (wb[q] & mb)) & mz;
+        const uint32_t s0 = z0 ? 0u : (uint32_t)((b0 ? eb0 : ea0) + 127);
+        const uint32_t s1 = z1 ? 0u : (uint32_t)((b1 ? eb1 : ea1) + 127);
+        *reinterpret_cast<uint16_t*>(rec + kCodeBytes + ((grp * 8 + p) * 4 + c) * 2) = (uint16_t)(s0 | (s1 << 8));
     }
     *reinterpret_cast<uint4*>(codes) = make_uint4(words[0], words[1], words[2], words[3]);
     *reinterpret_cast<uint4*>(codes + 16) = make_uint4(words[4], words[5], words[6], words[7]);

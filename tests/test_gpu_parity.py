@@ -107,6 +107,27 @@ def test_writer_rounding_ties():
     assert np.array_equal(gpu["pool"], ora["pool"])
 
 
+def test_writer_search_ties():
+    """Key blocks whose {4,6} squared errors tie exactly in binary32 (the
+    amax->6 scale is kept), and would flip to amax->4 if x - v*S were rounded
+    once (tests/golden/tie_blocks.json): every key block of two pages is one
+    of them, at every lane and token position."""
+    import json
+    import os
+    fx = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tie_blocks.json")))
+    blocks = torch.tensor(fx["blocks_bf16"], dtype=torch.int32)                # [n][16]
+    spec = cases.Spec(lens=[16 + 128 * 2], seed=52, rotation=0, centering=0, key_search=1)
+    c = cases.build(spec)
+    n_blk = c.k_pages.numel() // 16
+    idx = (torch.arange(n_blk) * 7) % blocks.shape[0]
+    kp = blocks[idx].to(torch.int16).view(torch.bfloat16).reshape(c.k_pages.shape)
+    c.k_pages = kp.contiguous()
+    c.gk = fx["g"]
+    gpu = cases.run_gpu(c)
+    ora = cases.run_oracle(c, pool_only=True)
+    assert np.array_equal(gpu["pool"], ora["pool"])
+
+
 def test_writer_extreme_scales():
     """Tiny and huge per-tensor scales: E4M3 subnormal and saturated block scales."""
     for gk, gv in ((1e-4, 3e-5), (10.0, 50.0), (1e-30, 1e30)):

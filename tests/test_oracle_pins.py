@@ -236,6 +236,34 @@ def test_four_six_brute_force():
     assert 200 < n4 < 3800     # both candidates are actually exercised
 
 
+def test_four_six_tie_fixture():
+    """tests/golden/tie_blocks.json holds blocks whose two squared-error sums
+    are equal in binary32: the oracle keeps amax->6 (ties keep the default),
+    and each block would flip to amax->4 if the reconstruction error were
+    rounded once (x - v*S as one fused operation) -- the fixture separates
+    the two-rounding reading from the fused one."""
+    import importlib.util
+    here = os.path.join(os.path.dirname(__file__), "golden")
+    spec = importlib.util.spec_from_file_location("make_tie_blocks", os.path.join(here, "make_tie_blocks.py"))
+    gen = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(gen)
+    fx = json.load(open(os.path.join(here, "tie_blocks.json")))
+    g = fx["g"]
+    assert len(fx["blocks_bf16"]) >= 32
+    for blk in fx["blocks_bf16"]:
+        x = (np.array(blk, np.uint32) << 16).view(np.float32)
+        m, codes, sb, xh, e4, e6 = oracle.four_six_block(x, g)
+        assert e4 == e6 and m == 6
+        c6, s6, x6 = oracle.nvfp4_block(x, 6, g)
+        c4, s4, x4 = oracle.nvfp4_block(x, 4, g)
+        assert sb == s6 and np.array_equal(codes, c6)
+        S6 = float(np.float32(oracle.e4m3_value([s6])[0]) * np.float32(g))
+        S4 = float(np.float32(oracle.e4m3_value([s4])[0]) * np.float32(g))
+        v6, v4 = oracle.e2m1_value(c6), oracle.e2m1_value(c4)
+        assert np.array_equal(xh, (v6 * np.float32(S6)).astype(np.float32))
+        assert gen.fused_sse(x, v4, S4) < gen.fused_sse(x, v6, S6)
+
+
 def test_mx_block_brute_force():
     rng = np.random.default_rng(10)
     for trial in range(1500):
