@@ -1010,6 +1010,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         qa.centering = a.centering;
         qa.terms = a.terms;
         qa.stride = a.qstride;
+        qa.zero_addend = a.zero_addend;
         qquant::quantize_token<1>(qa, a.q + (size_t)b * a.hq * kD, a.mu, smem + kQpOff, (int)threadIdx.x, kThreads,
                                   ctl->qred, [] { __syncthreads(); });
         __syncthreads();   // the record is complete

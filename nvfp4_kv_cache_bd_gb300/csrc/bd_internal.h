@@ -57,6 +57,7 @@ struct QueryArgs {
     uint8_t* qp;
     int B, hq, format, rotation, centering, terms;
     size_t stride;
+    float zero_addend = -0.0f;   // as in WriterArgs
 };
 
 struct DecodeArgs {
@@ -81,6 +82,7 @@ struct DecodeArgs {
     int pool_pages;           // 0: only negative block-table entries are rejected
     int format, centering, p_mode, p_c;
     float tau, gk, gv;
+    float zero_addend = -0.0f;   // as in WriterArgs (fused query quantization)
 };
 
 cudaError_t launch_writer(const WriterArgs& a, cudaStream_t s);

@@ -40,16 +40,18 @@ __device__ __forceinline__ float group_max(float v, float* red, int tid, int nth
     return r;
 }
 
-// One term: quantize this lane's 16 values x (NVFP4: a whole block; MXFP4:
-// half of a 32-block shared with lane c^1), store codes and scale bytes (when
-// `store`) and return the reconstruction in xh.
-__device__ __forceinline__ void quant_term(const QueryArgs& a, const float* x, float g, uint8_t* qp, int term, int j,
-                                           int c, float* xh, bool store) {
+// One term: quantize this lane's 16 values, held as pairs xp[i] = (x[2i],
+// x[2i+1]) (NVFP4: a whole block; MXFP4: half of a 32-block shared with lane
+// c^1), store codes and scale bytes (when `store`) and return the
+// reconstruction in xh.  z: the run-time -0.0f of mulz2 in both lanes.
+__device__ __forceinline__ void quant_term(const QueryArgs& a, const float2* xp, float g, float2 z, uint8_t* qp,
+                                           int term, int j, int c, float2* xh, bool store) {
     const int hq = a.hq;
     uint32_t w0 = 0, w1 = 0, sb;
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(xp[i].x), fabsf(xp[i].y)));
+    float2 S2;
     if (a.format == BD_FORMAT_NVFP4) {
         const float t = __fmul_rn(6.0f, g);
         const float s = __fdiv_rn(amax, t);
@@ -57,58 +59,51 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float* x, f
         const float S = __fmul_rn(e4m3_value(sb), g);
         const float inv = __frcp_rn(S);
         const bool zero = (S == 0.0f) || isinf(inv);
+        const float2 inv2 = splat2(inv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint32_t byte = zero ? 0u : e2m1x2(__fmul_rn(x[2 * i], inv), __fmul_rn(x[2 * i + 1], inv));
+            const float2 q = mul2(xp[i], inv2);
+            const uint32_t byte = e2m1x2(q.x, q.y);
             if (i < 4) w0 |= byte << (8 * i);
             else w1 |= byte << (8 * (i - 4));
-            float2 val = f16x2_to_float2(e2m1x2_to_f16x2(byte));
-            xh[2 * i] = zero ? 0.0f : __fmul_rn(val.x, S);
-            xh[2 * i + 1] = zero ? 0.0f : __fmul_rn(val.y, S);
         }
+        if (zero) {   // codes 0, so x_hat = +0 * S = +0
+            w0 = 0;
+            w1 = 0;
+        }
+        S2 = splat2(S);
         if (store) qp[2 * hq * 64 + (term * hq + j) * 8 + c] = (uint8_t)sb;
     } else {
         const float amax32 = fmaxf(amax, __shfl_xor_sync(kQFull, amax, 1));
         const int E = ilog2f(amax32 == 0.0f ? 1.0f : amax32);
         const int ea = min(127, max(-127, E - 2)), eb = min(127, max(-127, E - 1));
         float sse[2];
+        uint32_t ca0, ca1, cb0, cb1;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const int e = k ? eb : ea;
-            const float down = pow2i(-e), up = pow2i(e);
-            float w[16];
+            float2 wp[8];
+            if (k == 0) mx_enc_err16x2(xp, ea, z, ca0, ca1, wp);
+            else mx_enc_err16x2(xp, eb, z, cb0, cb1, wp);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t byte = e2m1x2(__fmul_rn(x[2 * i], down), __fmul_rn(x[2 * i + 1], down));
-                float2 val = f16x2_to_float2(e2m1x2_to_f16x2(byte));
-                float e0 = __fsub_rn(x[2 * i], __fmul_rn(val.x, up));
-                float e1 = __fsub_rn(x[2 * i + 1], __fmul_rn(val.y, up));
-                w[2 * i] = __fmul_rn(e0, e0);
-                w[2 * i + 1] = __fmul_rn(e1, e1);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __fadd_rn(w[i], __shfl_xor_sync(kQFull, w[i], 1));
-#pragma unroll
-            for (int hh = 8; hh >= 1; hh >>= 1)
-#pragma unroll
-                for (int i = 0; i < hh; ++i) w[i] = __fadd_rn(w[i], w[i + hh]);
-            sse[k] = w[0];
+            for (int i = 0; i < 8; ++i)
+                wp[i] = add2(wp[i], make_float2(__shfl_xor_sync(kQFull, wp[i].x, 1), __shfl_xor_sync(kQFull, wp[i].y, 1)));
+            sse[k] = tree16x2(wp);
         }
-        const bool zero = amax32 == 0.0f;
-        const int e = (sse[1] < sse[0]) ? eb : ea;
-        const float down = pow2i(-e), up = pow2i(e);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t byte = zero ? 0u : e2m1x2(__fmul_rn(x[2 * i], down), __fmul_rn(x[2 * i + 1], down));
-            if (i < 4) w0 |= byte << (8 * i);
-            else w1 |= byte << (8 * (i - 4));
-            float2 val = f16x2_to_float2(e2m1x2_to_f16x2(byte));
-            xh[2 * i] = zero ? 0.0f : __fmul_rn(val.x, up);
-            xh[2 * i + 1] = zero ? 0.0f : __fmul_rn(val.y, up);
-        }
+        const bool zero = amax32 == 0.0f;   // codes 0 and x_hat = +0
+        const bool pickb = sse[1] < sse[0];
+        const int e = pickb ? eb : ea;
+        w0 = zero ? 0u : (pickb ? cb0 : ca0);
+        w1 = zero ? 0u : (pickb ? cb1 : ca1);
+        S2 = splat2(pow2i(e));
         sb = zero ? 0u : (uint32_t)(e + 127);
         if (store && !(c & 1)) qp[2 * hq * 64 + (term * hq + j) * 4 + (c >> 1)] = (uint8_t)sb;
     }
+    // x_hat = value(code) * S, rounded once per element
+    uint32_t hv[8];
+    e2m1x8_to_f16x2x4(w0, hv);
+    e2m1x8_to_f16x2x4(w1, hv + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xh[i] = mulz2(f16x2_to_float2(hv[i]), S2, z);
     if (store) *reinterpret_cast<uint2*>(qp + (term * hq + j) * 64 + 8 * c) = make_uint2(w0, w1);
 }
 
@@ -122,7 +117,8 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
                                float* red, Sync sync) {
     const int hq = a.hq;
     const int c = tid & 7;
-    float x[NI][16];
+    const float2 z = splat2(a.zero_addend);
+    float2 x[NI][8];   // the item's 16 values as pairs (2i, 2i+1)
     float qmu[NI];
     bool act[NI];
     int jh[NI];
@@ -137,13 +133,10 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
             uint4 u1 = *reinterpret_cast<const uint4*>(src + 8);
             const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[n][2 * i] = bf16_lo(wd[i]);
-                x[n][2 * i + 1] = bf16_hi(wd[i]);
-            }
+            for (int i = 0; i < 8; ++i) x[n][i] = make_float2(bf16_lo(wd[i]), bf16_hi(wd[i]));
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[n][i] = 0.0f;
+            for (int i = 0; i < 8; ++i) x[n][i] = make_float2(0.0f, 0.0f);
         }
         // q.mu on the unrotated query (fp32, lane-partial then a 3-step butterfly)
         qmu[n] = 0.0f;
@@ -152,10 +145,10 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float4 v = m4[i];
-                qmu[n] = fmaf(x[n][4 * i], v.x, qmu[n]);
-                qmu[n] = fmaf(x[n][4 * i + 1], v.y, qmu[n]);
-                qmu[n] = fmaf(x[n][4 * i + 2], v.z, qmu[n]);
-                qmu[n] = fmaf(x[n][4 * i + 3], v.w, qmu[n]);
+                qmu[n] = fmaf(x[n][2 * i].x, v.x, qmu[n]);
+                qmu[n] = fmaf(x[n][2 * i].y, v.y, qmu[n]);
+                qmu[n] = fmaf(x[n][2 * i + 1].x, v.z, qmu[n]);
+                qmu[n] = fmaf(x[n][2 * i + 1].y, v.w, qmu[n]);
             }
         }
         qmu[n] += __shfl_xor_sync(kQFull, qmu[n], 1);
@@ -163,28 +156,36 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
         qmu[n] += __shfl_xor_sync(kQFull, qmu[n], 4);
 
         if (a.rotation) {
+            // stride 1 inside each pair
 #pragma unroll
-            for (int hs = 1; hs < 16; hs <<= 1)
+            for (int i = 0; i < 8; ++i) {
+                const float u = x[n][i].x, v = x[n][i].y;
+                x[n][i] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
+            }
+            // strides 2, 4, 8 between pairs
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
+            for (int hs = 1; hs < 8; hs <<= 1)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
                     if (!(i & hs)) {
-                        float u = x[n][i], v = x[n][i + hs];
-                        x[n][i] = __fadd_rn(u, v);
-                        x[n][i + hs] = __fsub_rn(u, v);
+                        const float2 u = x[n][i], v = x[n][i + hs];
+                        x[n][i] = add2(u, v);
+                        x[n][i + hs] = sub2(u, v);
                     }
 #pragma unroll
             for (int m = 1; m <= 4; m <<= 1) {
                 // p - x in the upper lane, x + p in the lower one: fma(x, +-1, p)
                 // rounds the exact p +- x once, like the add or subtract
-                const float sgn = (c & m) ? -1.0f : 1.0f;
+                const float2 sgn = splat2((c & m) ? -1.0f : 1.0f);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p = __shfl_xor_sync(kQFull, x[n][i], m);
-                    x[n][i] = __fmaf_rn(x[n][i], sgn, p);
+                for (int i = 0; i < 8; ++i) {
+                    const float2 p = make_float2(__shfl_xor_sync(kQFull, x[n][i].x, m),
+                                                 __shfl_xor_sync(kQFull, x[n][i].y, m));
+                    x[n][i] = fma2(x[n][i], sgn, p);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[n][i] = __fmul_rn(x[n][i], kRot);
+            for (int i = 0; i < 8; ++i) x[n][i] = mulz2(x[n][i], splat2(kRot), z);
         }
     }
 
@@ -192,13 +193,13 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
 #pragma unroll
     for (int n = 0; n < NI; ++n)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[n][i]));
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[n][i].x), fabsf(x[n][i].y)));
     amax = group_max(amax, red, tid, nthr, sync);
     float g1 = 1.0f;
     if (a.format == BD_FORMAT_NVFP4 && amax != 0.0f) g1 = __fdiv_rn(amax, 2688.0f);
-    float xh[NI][16];
+    float2 xh[NI][8];
 #pragma unroll
-    for (int n = 0; n < NI; ++n) quant_term(a, x[n], g1, qp, 0, jh[n], c, xh[n], act[n]);
+    for (int n = 0; n < NI; ++n) quant_term(a, x[n], g1, z, qp, 0, jh[n], c, xh[n], act[n]);
 
     float g2 = 0.0f;
     if (a.terms == 2) {
@@ -206,15 +207,15 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
 #pragma unroll
         for (int n = 0; n < NI; ++n)
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                x[n][i] = __fsub_rn(x[n][i], xh[n][i]);
-                amax_r = fmaxf(amax_r, fabsf(x[n][i]));
+            for (int i = 0; i < 8; ++i) {
+                x[n][i] = sub2(x[n][i], xh[n][i]);
+                amax_r = fmaxf(amax_r, fmaxf(fabsf(x[n][i].x), fabsf(x[n][i].y)));
             }
         amax_r = group_max(amax_r, red, tid, nthr, sync);
         g2 = 1.0f;
         if (a.format == BD_FORMAT_NVFP4 && amax_r != 0.0f) g2 = __fdiv_rn(amax_r, 2688.0f);
 #pragma unroll
-        for (int n = 0; n < NI; ++n) quant_term(a, x[n], g2, qp, 1, jh[n], c, xh[n], act[n]);
+        for (int n = 0; n < NI; ++n) quant_term(a, x[n], g2, z, qp, 1, jh[n], c, xh[n], act[n]);
     } else {
 #pragma unroll
         for (int n = 0; n < NI; ++n) {

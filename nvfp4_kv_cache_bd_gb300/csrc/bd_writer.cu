@@ -70,53 +70,6 @@ __device__ __forceinline__ void scale_tables(float g, float* stab) {
     }
 }
 
-// Two values -> one byte of E2M1 codes (lo in bits 3..0), and that byte
-// decoded back to f16x2 (exact), from one conversion register.
-__device__ __forceinline__ uint32_t e2m1x2_enc_dec(float lo, float hi, uint32_t& f16x2) {
-    uint32_t byte, h;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\tcvt.rn.f16x2.e2m1x2 %1, t;\n\t"
-        "cvt.u32.u8 %0, t;\n\t}"
-        : "=r"(byte), "=r"(h)
-        : "f"(hi), "f"(lo));
-    f16x2 = h;
-    return byte;
-}
-
-// Two-lane binary32 arithmetic: one packed instruction, each lane rounded to
-// nearest like the scalar add, subtract, multiply or fma.  The compiler has
-// been seen to fuse a packed multiply into a packed add or subtract that
-// consumes it (one rounding instead of two), .rn notwithstanding.  So every
-// product that is summed later is formed as fma(x, y, z) with z = -0.0f read
-// at run time (mulz2): exactly RN(x*y), and no single instruction can take
-// its place together with the sum.  Products that only feed a conversion or
-// another product stay plain multiplies (mul2).
-#define BD_F32X2_OP(name, op)                                                                      \
-    __device__ __forceinline__ float2 name(float2 a, float2 b) {                                   \
-        float2 r;                                                                                  \
-        asm("{\n\t.reg .b64 ra, rb, rr;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t" \
-            op " rr, ra, rb;\n\tmov.b64 {%0, %1}, rr;\n\t}"                                     \
-            : "=f"(r.x), "=f"(r.y)                                                                 \
-            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                             \
-        return r;                                                                                  \
-    }
-BD_F32X2_OP(add2, "add.rn.f32x2")
-BD_F32X2_OP(sub2, "sub.rn.f32x2")
-BD_F32X2_OP(mul2, "mul.rn.f32x2")
-#undef BD_F32X2_OP
-
-// a * b + c per lane, rounded once.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 r;
-    asm("{\n\t.reg .b64 ra, rb, rc, rr;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rr, ra, rb, rc;\n\tmov.b64 {%0, %1}, rr;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return r;
-}
-__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
-// a * b rounded once, for a product that a later add or subtract consumes;
-// z holds the run-time -0.0f (WriterArgs::zero_addend) in both lanes.
-__device__ __forceinline__ float2 mulz2(float2 a, float2 b, float2 z) { return fma2(a, b, z); }
 
 // Encode 8 pairs (elements 2i, 2i+1 in xp[i]) with scale (S, inv) into 8
 // code bytes (w0: elements 0-7, w1: 8-15) and fill wp[] with the squared
@@ -144,36 +97,6 @@ __device__ __forceinline__ void enc16x2(const float2* xp, float S, float inv, bo
     if (zero) {
         w0 = 0;
         w1 = 0;
-    }
-}
-
-// Squared-error tree over 16 terms w[i] += w[i+8], then +4, +2, +1, with the
-// terms held as pairs wp[i] = (w[2i], w[2i+1]): two additions per
-// instruction until the last.
-__device__ __forceinline__ float tree16x2(float2* wp) {
-#pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
-#pragma unroll
-        for (int i = 0; i < h; ++i) wp[i] = add2(wp[i], wp[i + h]);
-    return __fadd_rn(wp[0].x, wp[0].y);
-}
-
-// The 8 code bytes of the 8 pairs quantized with exponent e (w0: elements
-// 0-7, w1: 8-15) and their squared errors.
-__device__ __forceinline__ void mx_enc_err16x2(const float2* xp, int e, float2 z, uint32_t& w0, uint32_t& w1,
-                                               float2* wp) {
-    const float2 down = splat2(pow2i(-e)), up = splat2(pow2i(e));
-    w0 = 0;
-    w1 = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t hv;
-        const float2 q = mul2(xp[i], down);
-        const uint32_t byte = e2m1x2_enc_dec(q.x, q.y, hv);
-        if (i < 4) w0 |= byte << (8 * i);
-        else w1 |= byte << (8 * (i - 4));
-        const float2 err = sub2(xp[i], mulz2(f16x2_to_float2(hv), up, z));
-        wp[i] = mulz2(err, err, z);
     }
 }
 
