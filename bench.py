@@ -607,12 +607,12 @@ def main():
 # run of this bench; a launch's traffic does not depend on the layer count.
 # Valid only for the kernel code it was taken on: reported as null once the
 # hash of that code (comments and whitespace left out) differs.
-DECODE_TRAFFIC = {"sources_sha256_16": "855c128f222e9286", "ctx": 131072, "bytes": 151524352 + 3700480}
+DECODE_TRAFFIC = {"sources_sha256_16": "94b9f3440606fe48", "ctx": 131072, "bytes": 151526912 + 3669760}
 DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cuh")
 # Warp instructions one NVFP4 writer launch of the writer bench executes
 # (ncu smsp__inst_executed.sum, profiles/writer_kernel_64seq_page_fill.md),
 # for the writer's issue-rate roofline; null once its code changes.
-WRITER_INSTR = {"sources_sha256_16": "345cadbc6fabd91d", "fmt": 0, "warp_instructions": 10993664}
+WRITER_INSTR = {"sources_sha256_16": "1f89f52f52ebd7a2", "fmt": 0, "warp_instructions": 10993664}
 WRITER_SOURCES = ("bd_writer.cu", "bd_device.cuh", "bd_internal.h")
 
 
