@@ -514,17 +514,19 @@ def main():
 
     # ---------------- end to end through the C ABI with host buffers: one
     # host->device copy of the step's queries (all layers) from pinned memory,
-    # the layers, one device->host copy of the step's outputs
+    # the layers, one device->host copy of the step's outputs; both copies by
+    # bd_copy_async, a kernel that reads and writes the pinned host buffers
+    # over the CPU-GPU link
     q_host = torch.stack([q for q in wl.qs]).cpu().pin_memory()          # [layers][1][Hq][D] bf16
     out_host = torch.empty(args.layers, 1, HQ, D, dtype=torch.float32).pin_memory()
     q_dev = torch.empty_like(q_host, device=device)
     out_dev = torch.empty(args.layers, 1, HQ, D, dtype=torch.float32, device=device)
 
     def e2e_step():
-        q_dev.copy_(q_host, non_blocking=True)
+        bd.copy_async(q_dev, q_host)
         for l in range(args.layers):
             wl.layer(l, q=q_dev[l], out=out_dev[l])
-        out_host.copy_(out_dev, non_blocking=True)
+        bd.copy_async(out_host, out_dev)
 
     e2e_ms = timed(graphed(e2e_step, torch), args.steps, args.warmup, stream, torch, pg, clocks)
     e2e_ms = max_over_ranks(e2e_ms, pg, device)

@@ -314,6 +314,24 @@ int bd_decode_attention_noalloc(bd_ctx* ctx, int layer, const void* q_packed, co
  * recorded since the last read) and reset it to BD_OK. */
 int bd_read_device_error(bd_ctx* ctx, void* stream, int* out);
 
+/* Copy `bytes` bytes from src to dst by a kernel on `stream` (asynchronous).
+ * Each pointer is device memory of the current device or pinned host memory
+ * mapped at the same address (cudaHostAlloc / cudaHostRegister on a system
+ * with unified addressing); the kernel's loads and stores reach host memory
+ * through the CPU-GPU link.  On a Grace-Blackwell node this moves a decode
+ * step's queries in and its outputs out (a few hundred kilobytes) faster than
+ * a DMA copy, whose start-up dominates at that size.
+ *  - dst and src: 16-byte aligned; each range lies inside one allocation
+ *    (the call checks its two ends, not what lies between); the two ranges
+ *    must not overlap; any byte count (0 does nothing).
+ *  - The first and last byte of both ranges are checked with
+ *    cudaPointerGetAttributes before anything is launched: pageable host
+ *    memory, another device's memory, a null, unaligned or overlapping
+ *    range returns BD_ERR_INVALID_ARG and nothing is copied.
+ *  - Host memory written by the copy is complete once the stream reaches
+ *    the point after it (synchronize or wait on an event before reading). */
+int bd_copy_async(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier phase nothing will complete, for at most timeout_us microseconds
  * (1..2000000), then records BD_ERR_TIMEOUT in the device error word and

@@ -46,7 +46,7 @@ EXPORTS = ("bd_create", "bd_destroy", "bd_status_string", "bd_set_key_shift", "b
            "bd_query_packed_bytes", "bd_quantize_kv_pages", "bd_append_kv", "bd_quantize_query",
            "bd_decode_workspace_size",
            "bd_decode_attention", "bd_decode_attention_noalloc", "bd_read_device_error",
-           "bd_selftest_bounded_wait")
+           "bd_selftest_bounded_wait", "bd_copy_async")
 
 _lib = None
 
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "bd_decode_attention_noalloc": (I, [P, I, P, P, P, P, I, P, P, P, P, P, I, F, F, F, P, P]),
             "bd_read_device_error": (I, [P, P, ctypes.POINTER(I)]),
             "bd_selftest_bounded_wait": (I, [P, I, P]),
+            "bd_copy_async": (I, [P, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -222,6 +223,20 @@ def read_device_error(ctx: Context, stream=None) -> int:
     out = ctypes.c_int(0)
     _check(lib().bd_read_device_error(ctx.handle, _stream(stream), ctypes.byref(out)), "bd_read_device_error")
     return out.value
+
+
+def copy_async(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """bd_copy_async: copy src's bytes into dst by a kernel; each tensor is a
+    contiguous CUDA tensor or a contiguous pinned CPU tensor (same byte size)."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dst and src differ in size")
+    _check(lib().bd_copy_async(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "bd_copy_async")
 
 
 def selftest_bounded_wait(ctx: Context, timeout_us: int, stream=None):

@@ -9,6 +9,7 @@
 #include <new>
 #include <vector>
 
+#include "bd_copy.h"
 #include "bd_internal.h"
 
 struct bd_ctx {
@@ -356,6 +357,33 @@ int bd_read_device_error(bd_ctx* ctx, void* stream, int* out) {
     if (cudaMemset(ctx->d_err, 0, sizeof(int)) != cudaSuccess) return BD_ERR_CUDA;
     *out = v;
     return BD_OK;
+}
+
+int bd_copy_async(void* dst, const void* src, size_t bytes, void* stream) {
+    if (bytes == 0) return BD_OK;
+    if (!dst || !src) return BD_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15) return BD_ERR_INVALID_ARG;
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst), s0 = reinterpret_cast<uintptr_t>(src);
+    if (d0 < s0 + bytes && s0 < d0 + bytes) return BD_ERR_INVALID_ARG;   // overlapping ranges
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+    // first and last byte of each range: device memory of this device, or
+    // pinned host memory the device reaches at the same address
+    const void* ends[4] = {dst, static_cast<const uint8_t*>(dst) + bytes - 1, src,
+                           static_cast<const uint8_t*>(src) + bytes - 1};
+    for (const void* p : ends) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();   // an unknown pointer: clear the (non-sticky) error it left
+            return BD_ERR_INVALID_ARG;
+        }
+        const bool on_dev = at.type == cudaMemoryTypeDevice && at.device == dev;
+        const bool mapped_host = at.type == cudaMemoryTypeHost && at.devicePointer == p;
+        if (!on_dev && !mapped_host) return BD_ERR_INVALID_ARG;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BD_ERR_CUDA;
+    return cuda_status(bd::launch_copy(dst, src, bytes, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int bd_selftest_bounded_wait(bd_ctx* ctx, int timeout_us, void* stream) {

@@ -145,6 +145,15 @@ def test_null_and_range_arguments(L):
     assert L.bd_set_key_shift(h, 5, fake) == bd.ERR_INVALID_ARG
     assert L.bd_selftest_bounded_wait(h, 0, s) == bd.ERR_INVALID_ARG
     assert L.bd_read_device_error(h, s, None) == bd.ERR_INVALID_ARG
+    # copy: nothing to do, null, unaligned and overlapping ranges are settled
+    # before any CUDA call; a pointer CUDA does not know is refused after its
+    # attribute query (here: no GPU, so the query itself fails)
+    assert L.bd_copy_async(None, None, 0, s) == bd.OK
+    assert L.bd_copy_async(None, fake, 16, s) == bd.ERR_INVALID_ARG
+    assert L.bd_copy_async(fake, None, 16, s) == bd.ERR_INVALID_ARG
+    assert L.bd_copy_async(P(0x10008), P(0x20000), 16, s) == bd.ERR_INVALID_ARG
+    assert L.bd_copy_async(P(0x10000), P(0x10010), 32, s) == bd.ERR_INVALID_ARG
+    assert L.bd_copy_async(P(0x10000), P(0x20000), 64, s) in (bd.ERR_INVALID_ARG, bd.ERR_CUDA)
     ctx.close()
 
 
