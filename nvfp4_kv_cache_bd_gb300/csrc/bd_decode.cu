@@ -77,12 +77,14 @@ constexpr int kThreads = 256;
 constexpr int kMaxRec = 9216;                    // one K or V record (NVFP4; MXFP4 is 8704 B)
 constexpr int kNK = 4, kNV = 6;                  // K-ring and V-ring slots of kMaxRec bytes
 // With the query quantized inside the decode, the rings are filled with the
-// first round's K and V records (kPreK, kPreV pages) before the wait for the
-// preceding grid, the rest after it: the later V pages would only queue, in
-// the memory system, ahead of the preceding grid's merge and this grid's
-// query load (128K step: 1222 against 1238 µs with all ten slots filled
-// first; with fewer K pages, 1232-1261).
-constexpr int kPreK = 4, kPreV = 4;
+// first round's four K records and three of its V records (kPreK, kPreV
+// pages) before the wait for the preceding grid, the rest after it: later
+// pages would only queue, in the memory system, ahead of the preceding grid's
+// merge and this grid's query load, and the first round's last V page is
+// needed only after its scores.  128K step, one A/B each: all ten slots
+// 1238 against 1222 µs for 4 + 4; V pages 0 / 1 / 2 / 3 / 4 with four K
+// pages 1228 / 1224 / 1215 / 1212 / 1219; two K pages 1254.
+constexpr int kPreK = 4, kPreV = 3;
 static_assert(kPreK <= kNK && kPreV <= kNV, "pre-filled pages fit the rings");
 constexpr int kCtasPerSm = 2;
 // Register split of an FP4 split CTA: launched at kLaunchRegs per thread,
