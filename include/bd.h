@@ -329,7 +329,13 @@ int bd_read_device_error(bd_ctx* ctx, void* stream, int* out);
  *    memory, another device's memory, a null, unaligned or overlapping
  *    range returns BD_ERR_INVALID_ARG and nothing is copied.
  *  - Host memory written by the copy is complete once the stream reaches
- *    the point after it (synchronize or wait on an event before reading). */
+ *    the point after it (synchronize or wait on an event before reading).
+ *  - The kernel is a programmatic dependent launch, like this library's
+ *    other kernels: it lets the next kernel in the stream start early and
+ *    waits for the preceding grid before it reads src.  A kernel launched
+ *    after it with programmatic stream serialization must execute
+ *    griddepcontrol.wait before reading dst (this library's kernels do);
+ *    every other stream-ordered operation sees the copy complete. */
 int bd_copy_async(void* dst, const void* src, size_t bytes, void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an
