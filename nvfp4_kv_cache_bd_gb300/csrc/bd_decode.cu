@@ -1013,8 +1013,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         qa.terms = a.terms;
         qa.stride = a.qstride;
         qa.zero_addend = a.zero_addend;
+        // the operand image and the consumers need the second term and q.mu
+        // of this kv head's query heads only: thread items 32 h .. 32 h + 31,
+        // one whole warp
         qquant::quantize_token<1>(qa, a.q + (size_t)b * a.hq * kD, a.mu, smem + kQpOff, (int)threadIdx.x, kThreads,
-                                  ctl->qred, [] { __syncthreads(); });
+                                  ctl->qred, [] { __syncthreads(); }, kGroup * h, kGroup * h + kGroup);
         __syncthreads();   // the record is complete
     }
     // Each warpgroup keeps its own register share to the end: the control

@@ -112,9 +112,13 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float2* xp,
 // tid = 0..nthr-1, each taking the NI items it = tid + nthr i; items past
 // hq * 8 compute on zeros (they take part in the shuffles) and store
 // nothing.  mu: the layer's key mean [Hkv][128] (read only with centering).
+// The second term's codes and scale bytes, and q.mu, are produced only for
+// query heads j in [j2_lo, j2_hi) (both per-tensor scales still cover every
+// head); a caller that restricts them keeps each warp's heads all in or all
+// out.
 template <int NI, class Sync>
 __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const float* mu, uint8_t* qp, int tid, int nthr,
-                               float* red, Sync sync) {
+                               float* red, Sync sync, int j2_lo = 0, int j2_hi = 1 << 30) {
     const int hq = a.hq;
     const int c = tid & 7;
     const float2 z = splat2(a.zero_addend);
@@ -140,7 +144,7 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
         }
         // q.mu on the unrotated query (fp32, lane-partial then a 3-step butterfly)
         qmu[n] = 0.0f;
-        if (a.centering && mu && act[n]) {
+        if (a.centering && mu && act[n] && jh[n] >= j2_lo && jh[n] < j2_hi) {
             const float4* m4 = reinterpret_cast<const float4*>(mu + (jh[n] / kGroup) * kD + 16 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -215,7 +219,8 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
         g2 = 1.0f;
         if (a.format == BD_FORMAT_NVFP4 && amax_r != 0.0f) g2 = __fdiv_rn(amax_r, 2688.0f);
 #pragma unroll
-        for (int n = 0; n < NI; ++n) quant_term(a, x[n], g2, z, qp, 1, jh[n], c, xh[n], act[n]);
+        for (int n = 0; n < NI; ++n)
+            if (jh[n] >= j2_lo && jh[n] < j2_hi) quant_term(a, x[n], g2, z, qp, 1, jh[n], c, xh[n], act[n]);
     } else {
 #pragma unroll
         for (int n = 0; n < NI; ++n) {
@@ -236,7 +241,7 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
     }
 #pragma unroll
     for (int n = 0; n < NI; ++n)
-        if (act[n] && c == 0) reinterpret_cast<float*>(qp + goff + 16)[jh[n]] = qmu[n];
+        if (act[n] && c == 0 && jh[n] >= j2_lo && jh[n] < j2_hi) reinterpret_cast<float*>(qp + goff + 16)[jh[n]] = qmu[n];
     // zero the bytes no field covers: the unused half of the scale area in
     // MXFP4 and the tail after q.mu
     if (a.format == BD_FORMAT_MXFP4)
