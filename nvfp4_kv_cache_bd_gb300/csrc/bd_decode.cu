@@ -999,6 +999,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
             const uint64_t policy = l2_evict_first_policy();
             for (int k = 0; k < min(n, isK ? kPreK : kPreV); ++k) fill_slot<FMT>(a, h, bt, smem, ctl, isK, k, policy);
         }
+        // the warp whose items are this kv head's query heads reads their key
+        // mean now: it is in device memory before the kernel starts
+        // (bd_set_key_shift returns once it has landed), and a read after the
+        // wait would queue behind the ring fill
+        qquant::MuPre mu_pre{};
+        mu_pre.ok = warp == h && a.centering && a.mu;
+        if (mu_pre.ok) {
+            const float4* m4 = reinterpret_cast<const float4*>(a.mu + (size_t)h * kD + 16 * (lane & 7));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mu_pre.v[i] = m4[i];
+        }
         __syncwarp();
         griddep_wait();   // q may come from the preceding grid
         QueryArgs qa;
@@ -1017,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
         // of this kv head's query heads only: thread items 32 h .. 32 h + 31,
         // one whole warp
         qquant::quantize_token<1>(qa, a.q + (size_t)b * a.hq * kD, a.mu, smem + kQpOff, (int)threadIdx.x, kThreads,
-                                  ctl->qred, [] { __syncthreads(); }, kGroup * h, kGroup * h + kGroup);
+                                  ctl->qred, [] { __syncthreads(); }, kGroup * h, kGroup * h + kGroup, mu_pre);
         __syncthreads();   // the record is complete
     }
     // Each warpgroup keeps its own register share to the end: the control

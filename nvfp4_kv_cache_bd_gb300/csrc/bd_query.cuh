@@ -115,10 +115,18 @@ __device__ __forceinline__ void quant_term(const QueryArgs& a, const float2* xp,
 // The second term's codes and scale bytes, and q.mu, are produced only for
 // query heads j in [j2_lo, j2_hi) (both per-tensor scales still cover every
 // head); a caller that restricts them keeps each warp's heads all in or all
-// out.
+// out.  mu_pre.ok: mu_pre.v holds this thread's 16 key-mean values
+// (mu[j / 4][16 c .. 16 c + 15] of its single item, NI = 1), loaded by the
+// caller ahead of time; otherwise they are read from mu here.
+struct MuPre {
+    float4 v[4];
+    bool ok;
+};
+
 template <int NI, class Sync>
 __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const float* mu, uint8_t* qp, int tid, int nthr,
-                               float* red, Sync sync, int j2_lo = 0, int j2_hi = 1 << 30) {
+                               float* red, Sync sync, int j2_lo = 0, int j2_hi = 1 << 30,
+                               MuPre mu_pre = MuPre{}) {
     const int hq = a.hq;
     const int c = tid & 7;
     const float2 z = splat2(a.zero_addend);
@@ -148,7 +156,7 @@ __device__ void quantize_token(const QueryArgs& a, const uint16_t* qt, const flo
             const float4* m4 = reinterpret_cast<const float4*>(mu + (jh[n] / kGroup) * kD + 16 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 v = m4[i];
+                const float4 v = (NI == 1 && mu_pre.ok) ? mu_pre.v[i] : m4[i];
                 qmu[n] = fmaf(x[n][2 * i].x, v.x, qmu[n]);
                 qmu[n] = fmaf(x[n][2 * i].y, v.y, qmu[n]);
                 qmu[n] = fmaf(x[n][2 * i + 1].x, v.z, qmu[n]);
