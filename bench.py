@@ -609,7 +609,7 @@ def main():
 # run of this bench; a launch's traffic does not depend on the layer count.
 # Valid only for the kernel code it was taken on: reported as null once the
 # hash of that code (comments and whitespace left out) differs.
-DECODE_TRAFFIC = {"sources_sha256_16": "37c3d99406020f0e", "ctx": 131072, "bytes": 151524352 + 3850496}
+DECODE_TRAFFIC = {"sources_sha256_16": "7656eab6e85792c2", "ctx": 131072, "bytes": 151523328 + 3516160}
 DECODE_SOURCES = ("bd_decode.cu", "bd_device.cuh", "bd_internal.h", "bd_query.cuh")
 # Warp instructions one NVFP4 writer launch of the writer bench executes
 # (ncu smsp__inst_executed.sum, profiles/writer_kernel_64seq_page_fill.md),
