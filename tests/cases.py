@@ -31,6 +31,7 @@ class Spec:
     shuffle: bool = True
     spare_pages: int = 2
     pool_pages: int = 0    # declared pool size (0: not declared)
+    hkv: int = H           # kv heads (query heads: 4 per kv head)
 
 
 class Case:
@@ -44,6 +45,7 @@ def u16(t: torch.Tensor) -> np.ndarray:
 def build(spec: Spec, ctx=None) -> Case:
     c = Case()
     c.spec = spec
+    H, HQ = spec.hkv, 4 * spec.hkv
     B = len(spec.lens)
     mu, mask = synth.key_mean(H, spec.seed)
     c.mu = mu
@@ -89,11 +91,13 @@ def build(spec: Spec, ctx=None) -> Case:
     if c.gv == 0.0:
         c.gv = 1.0
     c.nphys = nphys
-    c.ocfg = oracle.make_config(fmt=spec.fmt, key_search=spec.key_search, rotation=spec.rotation,
+    c.ocfg = oracle.make_config(num_q_heads=HQ, num_kv_heads=H, fmt=spec.fmt, key_search=spec.key_search,
+                                rotation=spec.rotation,
                                 centering=spec.centering, query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c,
                                 pool_pages=spec.pool_pages)
     c.ctx = ctx if ctx is not None else bd.Context(bd.make_config(
-        format=spec.fmt, key_search=spec.key_search, rotation=spec.rotation, centering=spec.centering,
+        num_q_heads=HQ, num_kv_heads=H, format=spec.fmt, key_search=spec.key_search, rotation=spec.rotation,
+        centering=spec.centering,
         query_terms=spec.terms, p_mode=spec.p_mode, p_c=spec.p_c, pool_pages=spec.pool_pages))
     c.rec = oracle.record_bytes(c.ocfg)
     c.qstride = oracle.qpack_stride(c.ocfg)
@@ -102,6 +106,7 @@ def build(spec: Spec, ctx=None) -> Case:
 
 def strip_qmu(c: Case, qp: np.ndarray) -> np.ndarray:
     """Packed query bytes with the fp32 q.mu field zeroed (it is compared with a tolerance)."""
+    HQ = 4 * c.spec.hkv
     qp = qp.copy()
     off = 2 * HQ * 64 + 2 * HQ * 8 + 16
     qp[:, off:off + 4 * HQ] = 0
@@ -109,6 +114,7 @@ def strip_qmu(c: Case, qp: np.ndarray) -> np.ndarray:
 
 
 def qmu_of(c: Case, qp: np.ndarray) -> np.ndarray:
+    HQ = 4 * c.spec.hkv
     off = 2 * HQ * 64 + 2 * HQ * 8 + 16
     return np.ascontiguousarray(qp[:, off:off + 4 * HQ]).view(np.float32)
 
@@ -118,6 +124,7 @@ def run_gpu(c: Case, dev="cuda", stream=None, pool=None, fused_query=False) -> d
     decode takes no packed query and quantizes q itself (the packed query is
     still produced, for the fields compared elsewhere)."""
     B = len(c.spec.lens)
+    H, HQ = c.spec.hkv, 4 * c.spec.hkv
     bd.set_key_shift(c.ctx, 0, c.mu)
     g = lambda t: t.to(dev)
     if pool is None:
@@ -145,6 +152,7 @@ def run_gpu(c: Case, dev="cuda", stream=None, pool=None, fused_query=False) -> d
 
 
 def run_oracle(c: Case, pool_only: bool = False) -> dict:
+    H = c.spec.hkv
     pool = np.full(c.nphys * H * 2 * c.rec, FILL, np.uint8)
     if len(c.dst):
         oracle.quantize_kv_pages(c.ocfg, u16(c.k_pages), u16(c.v_pages), c.dst, c.mu.numpy(), c.gk, c.gv, pool)

@@ -374,6 +374,22 @@ def test_fused_query_matches_the_two_calls(fmt, rotation, centering, terms):
     assert mx < MAX_ABS and rl < REL_L2
 
 
+@pytest.mark.parametrize("hkv", [1, 2, 4])
+def test_fused_query_with_fewer_kv_heads(hkv):
+    """With fewer kv heads the token has fewer query heads than the decode
+    CTA has threads: the items past 4 * hkv heads compute on zeros, and the
+    warp whose items are the CTA's own query heads (warp h) still covers
+    them whole.  Fused output bit-identical to the two calls, and within
+    the oracle's tolerance."""
+    c = cases.build(cases.Spec(lens=[16 + 128 * 5 + 9, 16 + 128 * 2], seed=170 + hkv, hkv=hkv))
+    two = cases.run_gpu(c)
+    one = cases.run_gpu(c, fused_query=True)
+    assert np.array_equal(one["out"], two["out"]), np.nanmax(np.abs(one["out"] - two["out"]))
+    ora = cases.run_oracle(c)
+    mx, rl = cases.attn_errors(one["out"], ora["out"])
+    assert mx < MAX_ABS and rl < REL_L2
+
+
 def test_fused_query_on_a_multi_wave_grid():
     """20 sequences x 8 kv heads x (1 + 1) splits exceed one wave of two CTAs
     per SM: without a packed query the call quantizes it with the query
