@@ -20,8 +20,10 @@ decode-token append.  --no-configs keeps only the headline.
 
 Inputs are seeded synthetic tensors (nvfp4_kv_cache_bd_gb300.synth) resident
 in HBM before timing; every decode step streams more distinct pool bytes than
-L2 holds (asserted), so no explicit flush is needed.  Prints ONE JSON line on
-rank 0.
+L2 holds (asserted), so no explicit flush is needed.  The "e2e" figure times
+the same step with all layers' queries copied in from pinned host memory and
+all outputs copied out, both by bd_copy_async, inside the timed graph.
+Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
